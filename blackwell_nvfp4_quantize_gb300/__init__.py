@@ -1,0 +1,233 @@
+"""Direct-P FP4 attention forward for GB300 (sm_103a).
+
+Thin Python binding over the C ABI of ``libfp4attn.so`` (declared in
+``include/fp4attn.h``).  PyTorch supplies device memory and streams only; every
+step of the computation runs in the library's CUDA kernels.  The binding
+raises if the library has not been built -- there is no fallback.
+
+Method: "Hardware-Aware FP4 FlashAttention-4" (Direct-P for noncausal
+inference): NVFP4 Q/K, MXFP4 V along keys, scores mapped directly to MXFP4
+E2M1 probability codes, denominator from the same rounded probabilities, O
+and LSE as outputs.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfp4attn.so")
+
+FP4ATTN_OK = 0
+FP4ATTN_ERR_INVALID_ARG = 1
+FP4ATTN_ERR_UNSUPPORTED = 2
+FP4ATTN_ERR_CUDA = 3
+FP4ATTN_ERR_TIMEOUT = 4
+
+_lib = None
+
+
+class Fp4AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (what, status_string(status), status))
+
+
+class _NVFP4(ctypes.Structure):
+    _fields_ = [("payload", ctypes.c_void_p), ("sf", ctypes.c_void_p), ("g", ctypes.c_void_p)]
+
+
+class _MXFP4(ctypes.Structure):
+    _fields_ = [("payload_t", ctypes.c_void_p), ("sf", ctypes.c_void_p)]
+
+
+def lib():
+    """The loaded C library (ctypes.CDLL).  Raises if it is not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libfp4attn.so is not built (%s); run __graft_entry__.build() or "
+                           "python -m blackwell_nvfp4_quantize_gb300.build" % LIB_PATH)
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.fp4attn_status_string.argtypes = [i]
+    L.fp4attn_status_string.restype = ctypes.c_char_p
+    L.fp4attn_nvfp4_bytes.argtypes = [i, i, i, i, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+    L.fp4attn_mxfp4_v_bytes.argtypes = [i, i, i, i, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+    L.fp4attn_quant_qk_nvfp4.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
+    L.fp4attn_quant_v_mxfp4.argtypes = [vp, vp, vp, i, i, i, i, vp]
+    L.fp4attn_fwd_directp.argtypes = [ctypes.POINTER(_NVFP4), ctypes.POINTER(_NVFP4), ctypes.POINTER(_MXFP4),
+                                      vp, vp, i, i, i, i, f, vp]
+    L.fp4attn_debug_dump_p.argtypes = [ctypes.POINTER(_NVFP4), ctypes.POINTER(_NVFP4), ctypes.POINTER(_MXFP4),
+                                       vp, vp, i, i, i, i, f, i, i, i, i, vp, vp, vp]
+    L.fp4attn_device_status.argtypes = [vp]
+    L.fp4attn_debug_cvt_transitions.argtypes = [i, ctypes.c_uint32, ctypes.c_uint32, vp, i, vp, vp]
+    for name in ("fp4attn_debug_cvt_transitions", "fp4attn_nvfp4_bytes", "fp4attn_mxfp4_v_bytes", "fp4attn_quant_qk_nvfp4",
+                 "fp4attn_quant_v_mxfp4", "fp4attn_fwd_directp", "fp4attn_debug_dump_p",
+                 "fp4attn_device_status"):
+        getattr(L, name).restype = i
+    _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return lib().fp4attn_status_string(status).decode()
+
+
+def _check(status: int, what: str):
+    if status != FP4ATTN_OK:
+        raise Fp4AttnError(status, what)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+@dataclass
+class NVFP4Tensor:
+    """Q or K in NVFP4: payload [B,H,N,D/2] u8, scale atoms u8, g (1 fp32), on one device."""
+    payload: torch.Tensor
+    sf: torch.Tensor
+    g: torch.Tensor
+    shape: tuple
+
+    def _c(self):
+        return _NVFP4(self.payload.data_ptr(), self.sf.data_ptr(), self.g.data_ptr())
+
+
+@dataclass
+class MXFP4Tensor:
+    """V in MXFP4 along keys: payload_t [B,H,D,Npad/2] u8, scale atoms u8."""
+    payload_t: torch.Tensor
+    sf: torch.Tensor
+    shape: tuple
+
+    def _c(self):
+        return _MXFP4(self.payload_t.data_ptr(), self.sf.data_ptr())
+
+
+def nvfp4_bytes(B, H, N, D):
+    p, s = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().fp4attn_nvfp4_bytes(B, H, N, D, ctypes.byref(p), ctypes.byref(s)), "fp4attn_nvfp4_bytes")
+    return p.value, s.value
+
+
+def mxfp4_v_bytes(B, H, N, D):
+    p, s = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().fp4attn_mxfp4_v_bytes(B, H, N, D, ctypes.byref(p), ctypes.byref(s)), "fp4attn_mxfp4_v_bytes")
+    return p.value, s.value
+
+
+def _check_input(x: torch.Tensor, name: str):
+    if not (x.is_cuda and x.dtype == torch.bfloat16 and x.dim() == 4 and x.is_contiguous()):
+        raise ValueError("%s must be a contiguous CUDA bf16 tensor [B,H,N,D]" % name)
+
+
+def empty_nvfp4(shape, device) -> NVFP4Tensor:
+    B, H, N, D = shape
+    pb, sb = nvfp4_bytes(B, H, N, D)
+    return NVFP4Tensor(torch.empty((B, H, N, D // 2), dtype=torch.uint8, device=device),
+                       torch.empty((sb,), dtype=torch.uint8, device=device),
+                       torch.empty((1,), dtype=torch.float32, device=device), tuple(shape))
+
+
+def empty_mxfp4(shape, device) -> MXFP4Tensor:
+    B, H, N, D = shape
+    pb, sb = mxfp4_v_bytes(B, H, N, D)
+    npad = (N + 127) // 128 * 128
+    return MXFP4Tensor(torch.empty((B, H, D, npad // 2), dtype=torch.uint8, device=device),
+                       torch.empty((sb,), dtype=torch.uint8, device=device), tuple(shape))
+
+
+def quant_qk_nvfp4(x: torch.Tensor, out: NVFP4Tensor | None = None, stream=None) -> NVFP4Tensor:
+    """fp4attn_quant_qk_nvfp4 on a CUDA bf16 [B,H,N,D] tensor."""
+    _check_input(x, "x")
+    B, H, N, D = x.shape
+    out = out or empty_nvfp4(x.shape, x.device)
+    _check(lib().fp4attn_quant_qk_nvfp4(_ptr(x), _ptr(out.payload), _ptr(out.sf), _ptr(out.g),
+                                        B, H, N, D, ctypes.c_void_p(_stream(stream))), "fp4attn_quant_qk_nvfp4")
+    return out
+
+
+def quant_v_mxfp4(v: torch.Tensor, out: MXFP4Tensor | None = None, stream=None) -> MXFP4Tensor:
+    """fp4attn_quant_v_mxfp4 on a CUDA bf16 [B,H,N,D] tensor."""
+    _check_input(v, "v")
+    B, H, N, D = v.shape
+    out = out or empty_mxfp4(v.shape, v.device)
+    _check(lib().fp4attn_quant_v_mxfp4(_ptr(v), _ptr(out.payload_t), _ptr(out.sf), B, H, N, D,
+                                       ctypes.c_void_p(_stream(stream))), "fp4attn_quant_v_mxfp4")
+    return out
+
+
+def fwd_directp(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP4Tensor, softmax_scale: float | None = None,
+                o: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
+    """fp4attn_fwd_directp: returns (O bf16 [B,H,N,D], LSE fp32 [B,H,N])."""
+    B, H, N, D = q.shape
+    dev = q.payload.device
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    o = o if o is not None else torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev)
+    lse = lse if lse is not None else torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    qc, kc, vc = q._c(), k._c(), v._c()
+    _check(lib().fp4attn_fwd_directp(ctypes.byref(qc), ctypes.byref(kc), ctypes.byref(vc), _ptr(o), _ptr(lse),
+                                     B, H, N, D, float(softmax_scale), ctypes.c_void_p(_stream(stream))),
+           "fp4attn_fwd_directp")
+    return o, lse
+
+
+def debug_dump_p(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP4Tensor, b: int, h: int, row0: int, nrows: int,
+                 softmax_scale: float | None = None, stream=None):
+    """fp4attn_debug_dump_p: (O, LSE, codes [nrows, Npad/2] u8, kshift [nrows, Npad/32] i32)."""
+    B, H, N, D = q.shape
+    dev = q.payload.device
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    npad = (N + 127) // 128 * 128
+    o = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    codes = torch.zeros((nrows, npad // 2), dtype=torch.uint8, device=dev)
+    kshift = torch.zeros((nrows, npad // 32), dtype=torch.int32, device=dev)
+    qc, kc, vc = q._c(), k._c(), v._c()
+    _check(lib().fp4attn_debug_dump_p(ctypes.byref(qc), ctypes.byref(kc), ctypes.byref(vc), _ptr(o), _ptr(lse),
+                                      B, H, N, D, float(softmax_scale), b, h, row0, nrows, _ptr(codes),
+                                      _ptr(kshift), ctypes.c_void_p(_stream(stream))), "fp4attn_debug_dump_p")
+    return o, lse, codes, kshift
+
+
+def device_status(stream=None) -> int:
+    """fp4attn_device_status: FP4ATTN_OK, or FP4ATTN_ERR_TIMEOUT if a bounded wait gave up."""
+    return lib().fp4attn_device_status(ctypes.c_void_p(_stream(stream)))
+
+
+def debug_cvt_transitions(fmt: int, lo: int, hi: int, capacity: int = 4096, stream=None):
+    """fp4attn_debug_cvt_transitions: sorted list of (bit pattern, code) where the conversion changes."""
+    pairs = torch.zeros((capacity, 2), dtype=torch.int64).to(torch.int32).cuda()
+    count = torch.zeros((1,), dtype=torch.int32, device=pairs.device)
+    _check(lib().fp4attn_debug_cvt_transitions(fmt, lo, hi, _ptr(pairs), capacity, _ptr(count),
+                                               ctypes.c_void_p(_stream(stream))), "fp4attn_debug_cvt_transitions")
+    n = int(count.item())
+    if n > capacity:
+        raise RuntimeError("more transitions (%d) than capacity (%d)" % (n, capacity))
+    out = pairs[:n].cpu().numpy().view("uint32")
+    return sorted((int(a), int(b)) for a, b in out)
+
+
+def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scale: float | None = None, stream=None):
+    """Quantize Q, K (NVFP4) and V (MXFP4) and run the Direct-P forward: (O, LSE)."""
+    qq = quant_qk_nvfp4(q, stream=stream)
+    kq = quant_qk_nvfp4(k, stream=stream)
+    vq = quant_v_mxfp4(v, stream=stream)
+    return fwd_directp(qq, kq, vq, softmax_scale, stream=stream)

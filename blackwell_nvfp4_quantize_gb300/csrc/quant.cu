@@ -1,0 +1,224 @@
+// Quantizers of the Direct-P attention forward ("Hardware-Aware FP4
+// FlashAttention-4", section "What the paper found": Q and K in NVFP4, the PV
+// product on MXFP4 E2M1 operands).
+//
+//  amax_kernel        : |x| maximum of a bf16 tensor -> one fp32 (as bits) in g
+//  nvfp4_quant_kernel : 16-element blocks along D, E4M3 block scale, E2M1 codes
+//  nvfp4_finalize     : g = amax / 2688 (1 for an all-zero tensor)
+//  mxfp4_v_kernel     : 32-key blocks per channel, E8M0 scale, codes written
+//                       key-inner (V transposed) through shared memory
+//
+// All three data kernels are HBM-bound streaming passes: 16-byte vector loads,
+// grid sized in multiples of the SM count, warp-shuffle reductions, and
+// coalesced stores.  fp32 arithmetic uses explicitly rounded intrinsics so that
+// no multiply-add contraction changes a code.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace fp4attn {
+namespace {
+
+constexpr float kNvfp4GlobalDiv = 2688.0f;  // 6 (E2M1 max) * 448 (E4M3 max)
+
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  const uint32_t e = (code >> 3) & 15u, m = code & 7u;
+  if (e == 0) return static_cast<float>(m) * 0x1p-9f;  // exact
+  return __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+__device__ __forceinline__ float global_scale(float amax) {
+  return amax > 0.0f ? __fdiv_rn(amax, kNvfp4GlobalDiv) : 1.0f;
+}
+
+// Max of |bf16| over the 8 bf16 values of a 16-byte vector, as bf16 bits.
+__device__ __forceinline__ uint32_t absmax_vec(const uint4& v, uint32_t m2) {
+  m2 = __vmaxu2(m2, v.x & 0x7FFF7FFFu);
+  m2 = __vmaxu2(m2, v.y & 0x7FFF7FFFu);
+  m2 = __vmaxu2(m2, v.z & 0x7FFF7FFFu);
+  m2 = __vmaxu2(m2, v.w & 0x7FFF7FFFu);
+  return m2;
+}
+
+__global__ void __launch_bounds__(256) amax_kernel(const uint4* __restrict__ x, long long nvec,
+                                                   unsigned int* __restrict__ amax_bits) {
+  uint32_t m2 = 0;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < nvec; i += 4 * stride) {
+    const uint4 a = __ldcs(x + i), b = __ldcs(x + i + stride), c = __ldcs(x + i + 2 * stride),
+                d = __ldcs(x + i + 3 * stride);
+    m2 = absmax_vec(a, m2);
+    m2 = absmax_vec(b, m2);
+    m2 = absmax_vec(c, m2);
+    m2 = absmax_vec(d, m2);
+  }
+  for (; i < nvec; i += stride) m2 = absmax_vec(__ldcs(x + i), m2);
+  uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  __shared__ uint32_t red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    uint32_t v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0u;
+    v = __reduce_max_sync(0xFFFFFFFFu, v);
+    // non-negative floats order like their bit patterns
+    if (threadIdx.x == 0 && v != 0) atomicMax(amax_bits, v << 16);
+  }
+}
+
+// One thread per 16-element block; a warp covers 32 consecutive blocks, so
+// the 4 scale bytes of one atom word come from 4 neighbouring lanes.
+__global__ void __launch_bounds__(256) nvfp4_quant_kernel(const uint4* __restrict__ x, uint2* __restrict__ payload,
+                                                          uint8_t* __restrict__ sf, const float* __restrict__ amax_in,
+                                                          int N, int D, long long nblocks) {
+  const float g = global_scale(*amax_in);
+  const float six_g = __fmul_rn(6.0f, g);
+  const int kbs = D / 16;
+  const int ntiles = (N + 127) / 128;
+  const int lane = threadIdx.x & 31;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long base = static_cast<long long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+       base < nblocks; base += stride) {
+    const long long blk = base + lane;
+    const bool active = blk < nblocks;
+    uint32_t sb = 0;
+    if (active) {
+      const uint4 a = __ldcs(x + 2 * blk), b = __ldcs(x + 2 * blk + 1);
+      uint32_t m2 = absmax_vec(b, absmax_vec(a, 0u));
+      const float amax_b = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
+      sb = cvt_e4m3(__fdiv_rn(amax_b, six_g));
+      const float s = __fmul_rn(e4m3_value(sb), g);
+      uint2 out = make_uint2(0u, 0u);
+      if (s != 0.0f) {
+        const float inv = __frcp_rn(s);
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        float y[16];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          y[2 * k] = __fmul_rn(__uint_as_float(w[k] << 16), inv);
+          y[2 * k + 1] = __fmul_rn(__uint_as_float(w[k] & 0xFFFF0000u), inv);
+        }
+        out.x = cvt_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
+        out.y = cvt_e2m1x8(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]);
+      }
+      __stcs(payload + blk, out);
+    }
+    // gather the four scale bytes of one atom word into the lane with k == 0
+    uint32_t word = sb << (8 * (lane & 3));
+    word |= __shfl_xor_sync(0xFFFFFFFFu, word, 1);
+    word |= __shfl_xor_sync(0xFFFFFFFFu, word, 2);
+    if (active && (lane & 3) == 0) {
+      const long long row = blk / kbs;
+      const int kb = static_cast<int>(blk % kbs);
+      const long long bh = row / N;
+      const int n = static_cast<int>(row % N);
+      const int r = n & 127;
+      const long long atom = (bh * ntiles + n / 128) * (kbs / 4) + kb / 4;
+      *reinterpret_cast<uint32_t*>(sf + atom * 512 + (r & 31) * 16 + (r >> 5) * 4) = word;
+    }
+  }
+}
+
+__global__ void nvfp4_finalize_kernel(float* g) { *g = global_scale(*g); }
+
+// V [B,H,N,D] bf16 -> V^T codes [B,H,D,Npad/2] + E8M0 atoms.  One CTA per
+// (128-key tile, b*H+h).  The tile is staged in shared memory row-major;
+// lanes of a warp then take consecutive channels d of one 32-key block, so
+// each column read is conflict-free.
+template <int D>
+__global__ void __launch_bounds__(256) mxfp4_v_kernel(const uint4* __restrict__ v, uint8_t* __restrict__ payload_t,
+                                                      uint8_t* __restrict__ sf, int N) {
+  __shared__ __align__(16) uint16_t tile[128 * D];
+  __shared__ __align__(16) uint32_t atom[128];
+  const int kt = blockIdx.x;
+  const long long bh = blockIdx.y;
+  const int ntiles = gridDim.x;
+  const int npad_half = ntiles * 64;  // bytes per V^T row
+  constexpr int VPR = D / 8;          // 16-byte vectors per token row
+  for (int i = threadIdx.x; i < 128 * VPR; i += 256) {
+    const int r = i / VPR, cv = i % VPR;
+    const int n = kt * 128 + r;
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (n < N) val = __ldcs(v + ((bh * N + n) * VPR + cv));
+    *reinterpret_cast<uint4*>(&tile[r * D + cv * 8]) = val;
+  }
+  if (threadIdx.x < 128) atom[threadIdx.x] = 0u;
+  __syncthreads();
+  for (int pidx = threadIdx.x; pidx < 4 * D; pidx += 256) {
+    const int d = pidx % D, kb = pidx / D;
+    uint32_t h[32];
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      h[i] = tile[(kb * 32 + i) * D + d];
+      m = max(m, h[i] & 0x7FFFu);
+    }
+    // e = smallest integer >= -127 with amax <= 6 * 2^e, from the bits of amax
+    const uint32_t ebits = m >> 7, frac = m & 0x7Fu;  // bf16: 8 exponent, 7 mantissa bits
+    int e = -127;
+    if (ebits != 0) e = max(-127, static_cast<int>(ebits) - 127 - (frac <= 0x40u ? 2 : 1));
+    const float inv_scale = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, e <= 126
+    float y[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) y[i] = __fmul_rn(__uint_as_float(h[i] << 16), inv_scale);
+    uint4 out;
+    out.x = cvt_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
+    out.y = cvt_e2m1x8(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]);
+    out.z = cvt_e2m1x8(y[16], y[17], y[18], y[19], y[20], y[21], y[22], y[23]);
+    out.w = cvt_e2m1x8(y[24], y[25], y[26], y[27], y[28], y[29], y[30], y[31]);
+    __stcs(reinterpret_cast<uint4*>(payload_t + (bh * D + d) * npad_half + kt * 64 + kb * 16), out);
+    reinterpret_cast<uint8_t*>(atom)[(d & 31) * 16 + (d >> 5) * 4 + kb] = static_cast<uint8_t>(e + 127);
+  }
+  __syncthreads();
+  if (threadIdx.x < 32)
+    reinterpret_cast<uint4*>(sf + (bh * ntiles + kt) * 512)[threadIdx.x] =
+        reinterpret_cast<const uint4*>(atom)[threadIdx.x];
+}
+
+int grid_for(long long work_items, int threads) {
+  const long long want = (work_items + threads - 1) / threads;
+  const long long cap = static_cast<long long>(sm_count()) * 8;  // 8 x 256 threads per SM
+  return static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
+}
+
+}  // namespace
+}  // namespace fp4attn
+
+using namespace fp4attn;
+
+extern "C" int fp4attn_quant_qk_nvfp4(const void* x, uint8_t* payload, uint8_t* sf, float* g, int B, int H, int N,
+                                      int D, void* stream) {
+  int st = check_shape(B, H, N, D);
+  if (st != FP4ATTN_OK) return st;
+  if (!x || !payload || !sf || !g) return FP4ATTN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(payload) || !aligned16(sf) || !aligned16(g)) return FP4ATTN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const long long elems = static_cast<long long>(B) * H * N * D;
+  const long long nvec = elems / 8;
+  const long long nblocks = elems / 16;
+  cudaError_t e = cudaMemsetAsync(g, 0, sizeof(float), s);
+  if (e == cudaSuccess && (N % 128) != 0) e = cudaMemsetAsync(sf, 0, nvfp4_sf_bytes(B, H, N, D), s);
+  if (e != cudaSuccess) return FP4ATTN_ERR_CUDA;
+  amax_kernel<<<grid_for(nvec, 256 * 4), 256, 0, s>>>(static_cast<const uint4*>(x), nvec,
+                                                      reinterpret_cast<unsigned int*>(g));
+  nvfp4_quant_kernel<<<grid_for(nblocks, 256), 256, 0, s>>>(static_cast<const uint4*>(x),
+                                                             reinterpret_cast<uint2*>(payload), sf, g, N, D, nblocks);
+  nvfp4_finalize_kernel<<<1, 1, 0, s>>>(g);
+  return cuda_status(cudaGetLastError());
+}
+
+extern "C" int fp4attn_quant_v_mxfp4(const void* v, uint8_t* payload_t, uint8_t* sf, int B, int H, int N, int D,
+                                     void* stream) {
+  int st = check_shape(B, H, N, D);
+  if (st != FP4ATTN_OK) return st;
+  if (!v || !payload_t || !sf) return FP4ATTN_ERR_INVALID_ARG;
+  if (!aligned16(v) || !aligned16(payload_t) || !aligned16(sf)) return FP4ATTN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  dim3 grid(n_row_tiles(N), B * H);
+  if (D == 128)
+    mxfp4_v_kernel<128><<<grid, 256, 0, s>>>(static_cast<const uint4*>(v), payload_t, sf, N);
+  else
+    mxfp4_v_kernel<64><<<grid, 256, 0, s>>>(static_cast<const uint4*>(v), payload_t, sf, N);
+  return cuda_status(cudaGetLastError());
+}

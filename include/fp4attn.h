@@ -1,0 +1,153 @@
+/*
+ * fp4attn -- Direct-P FP4 attention forward for GB300 (sm_103a).
+ *
+ * C ABI of the CUDA library libfp4attn.so.  Every call takes plain device
+ * pointers and sizes, is asynchronous on the given CUDA stream (a
+ * cudaStream_t passed as void*, NULL = legacy default stream), validates its
+ * arguments on the host before launching anything, and returns an
+ * FP4ATTN_STATUS code.  The caller owns all input and output memory.  No call
+ * allocates device memory, except that the first call on a device sets up a
+ * 256-byte status word for that device (cudaMalloc once; see
+ * fp4attn_device_status).
+ *
+ * The operation follows "Hardware-Aware FP4 FlashAttention-4" (arXiv
+ * 2609.04105); sections cited are those of its neuraltrendhub.com summary
+ * page ("What the paper found") and of the abstract.  The method keeps Q and
+ * K in NVFP4, maps max-shifted log2 scores directly to MXFP4 E2M1
+ * probability codes, sums the softmax denominator from the same rounded
+ * probabilities that the PV product consumes, and emits O together with the
+ * LSE.  Where the pages fix no formula the library implements these readings:
+ *   NVFP4 (Q, K): 16-element blocks along D; g = amax(|x|)/2688 per tensor
+ *     (1 when all zero); block scale byte = E4M3(amax_b / (6 g)) (RNE,
+ *     saturating); codes = E2M1(x * fp32(1 / (dec(byte) * g))), RNE,
+ *     saturating, sign kept; a block whose scale decodes to 0 is all zero.
+ *   MXFP4 (V, along keys): 32-key blocks per (b, h, d); scale 2^e with e the
+ *     smallest integer >= -127 such that amax <= 6 * 2^e; codes = E2M1(v*2^-e).
+ *   Direct-P: c = fp32(softmax_scale * log2(e) * g_Q * g_K);
+ *     X = c * S (S the block-scaled FP4 product of the codes);
+ *     per 32-key block K_b = ceil(X_b - log2 6) with X_b the block maximum;
+ *     code = E2M1(2^(X - K_b)); the block's E8M0 scale is 2^(K_b - M) for an
+ *     integer reference maximum M (>= ceil of every score seen so far);
+ *     l = sum of the decoded probabilities; O = (P V) / l;
+ *     LSE = ln 2 * (M + log2 l), the natural-log log-sum-exp of
+ *     softmax_scale * (q . k) as seen through the quantized operands.
+ *
+ * Data layouts (all row-major, byte addressed):
+ *   bf16 inputs/outputs:  [B, H, N, D]
+ *   E2M1 packing:         element 2i in bits 0-3 of byte i, 2i+1 in bits 4-7
+ *   Q/K payload:          [B, H, N, D/2] bytes
+ *   V payload (keys inner, "transposed"): [B, H, D, Npad/2] bytes,
+ *                         Npad = N rounded up to a multiple of 128; keys >= N
+ *                         hold code 0
+ *   scale-factor atoms:   512 bytes cover 128 rows x 4 consecutive scale
+ *                         blocks; row r, block k of an atom is the byte at
+ *                         (r % 32) * 16 + (r / 32) * 4 + k
+ *     Q/K scales: atom [b*H + h][n / 128][block / 4], rows = tokens n,
+ *                 blocks = 16-element groups along D   (D/16 per token)
+ *     V scales:   atom [b*H + h][n / 128], rows = channels d (D <= 128,
+ *                 rows >= D are 0), blocks = 32-key groups of that tile
+ *   LSE:                  fp32 [B, H, N]
+ *
+ * Supported shapes: D in {64, 128}; B, H, N >= 1; B*H*N < 2^31.  The
+ * quantizers accept any N; fp4attn_fwd_directp accepts any N >= 1 (a partial
+ * last key tile is masked, a partial last query tile is not stored).
+ * All pointers must be 16-byte aligned.
+ */
+#ifndef FP4ATTN_H
+#define FP4ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    FP4ATTN_OK = 0,
+    FP4ATTN_ERR_INVALID_ARG = 1, /* null or misaligned pointer, bad size, non-finite scale */
+    FP4ATTN_ERR_UNSUPPORTED = 2, /* D not in {64, 128}, sizes beyond the supported range */
+    FP4ATTN_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+    FP4ATTN_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up (see fp4attn_device_status) */
+};
+
+/* Quantized NVFP4 tensor (Q or K) as written by fp4attn_quant_qk_nvfp4. */
+typedef struct {
+    const uint8_t *payload; /* [B,H,N,D/2] */
+    const uint8_t *sf;      /* scale atoms, fp4attn_nvfp4_bytes(...).sf bytes */
+    const float *g;         /* one fp32 tensor scale, in device memory */
+} fp4attn_nvfp4_t;
+
+/* Quantized MXFP4 V as written by fp4attn_quant_v_mxfp4. */
+typedef struct {
+    const uint8_t *payload_t; /* [B,H,D,Npad/2] */
+    const uint8_t *sf;        /* scale atoms, fp4attn_mxfp4_v_bytes(...).sf bytes */
+} fp4attn_mxfp4_t;
+
+/* Message for a status code (static string, never NULL). */
+const char *fp4attn_status_string(int status);
+
+/* Sizes in bytes of the NVFP4 buffers for a [B,H,N,D] tensor.
+ * Returns FP4ATTN_ERR_INVALID_ARG / _UNSUPPORTED for bad shapes. */
+int fp4attn_nvfp4_bytes(int B, int H, int N, int D, size_t *payload_bytes, size_t *sf_bytes);
+
+/* Sizes in bytes of the MXFP4 V buffers for a [B,H,N,D] tensor. */
+int fp4attn_mxfp4_v_bytes(int B, int H, int N, int D, size_t *payload_bytes, size_t *sf_bytes);
+
+/* NVFP4-quantize Q or K ("What the paper found": NVFP4 for Q and K).
+ * x: bf16 [B,H,N,D] (device, read only).  Writes payload, sf (every byte of
+ * the padded atoms) and *g (device, 4 bytes; used as the amax accumulator
+ * while the call runs).  Launches a memset and three kernels on stream;
+ * inputs must be finite. */
+int fp4attn_quant_qk_nvfp4(const void *x, uint8_t *payload, uint8_t *sf, float *g,
+                           int B, int H, int N, int D, void *stream);
+
+/* MXFP4-quantize V along the key axis, writing it key-inner
+ * ("What the paper found": MXFP4 E2M1 P/V operands of the PV product).
+ * v: bf16 [B,H,N,D].  Writes payload_t and sf (all bytes, padding included).
+ * One kernel; inputs must be finite. */
+int fp4attn_quant_v_mxfp4(const void *v, uint8_t *payload_t, uint8_t *sf,
+                          int B, int H, int N, int D, void *stream);
+
+/* Noncausal Direct-P forward (abstract: "Direct-P for noncausal inference";
+ * "What the paper found": E2M1 probability codes from log-softmax scores,
+ * denominator from the same rounded probabilities, LSE).
+ * q, k: quantized NVFP4 tensors; v: quantized MXFP4 V; o: bf16 [B,H,N,D];
+ * lse: fp32 [B,H,N].  softmax_scale must be finite and > 0.  One kernel
+ * launch on stream.  Returns FP4ATTN_ERR_TIMEOUT only from
+ * fp4attn_device_status; a launch returns OK or an argument/CUDA error. */
+int fp4attn_fwd_directp(const fp4attn_nvfp4_t *q, const fp4attn_nvfp4_t *k, const fp4attn_mxfp4_t *v,
+                        void *o, float *lse, int B, int H, int N, int D, float softmax_scale,
+                        void *stream);
+
+/* Same computation as fp4attn_fwd_directp (same kernel, same launch shape),
+ * and in addition writes the probability codes and block shifts of query
+ * rows row0 .. row0+nrows-1 of head (b, h):
+ *   codes:  [nrows, Npad/2] bytes, packed like the payloads (keys >= N are 0)
+ *   kshift: [nrows, Npad/32] int32 block shifts K_b (0 for blocks past N)
+ * For parity tests; O and LSE are written exactly as by the forward call. */
+int fp4attn_debug_dump_p(const fp4attn_nvfp4_t *q, const fp4attn_nvfp4_t *k, const fp4attn_mxfp4_t *v,
+                         void *o, float *lse, int B, int H, int N, int D, float softmax_scale,
+                         int b, int h, int row0, int nrows, uint8_t *codes, int32_t *kshift,
+                         void *stream);
+
+/* Test support (no counterpart in the method): for format 0 (E2M1) or 1
+ * (E4M3), converts every fp32 bit pattern u in [lo, hi] with the hardware
+ * round-to-nearest-even saturating conversion the library uses, and records
+ * into pairs[2i], pairs[2i+1] (device, capacity pairs) each pattern u > lo
+ * whose code differs from that of u-1, plus the pair (lo, code(lo)); *count
+ * (device int) receives the number of pairs found (may exceed capacity; the
+ * order of pairs is unspecified). */
+int fp4attn_debug_cvt_transitions(int format, uint32_t lo, uint32_t hi, uint32_t *pairs, int capacity,
+                                  int *count, void *stream);
+
+/* Reads and clears the status word the kernels of this library set when a
+ * bounded device-side wait gives up (they then stop early and leave their
+ * outputs incomplete).  Synchronises the given stream first.  Returns
+ * FP4ATTN_OK or FP4ATTN_ERR_TIMEOUT (or _CUDA if the readback fails). */
+int fp4attn_device_status(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
