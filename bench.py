@@ -1,0 +1,356 @@
+#!/usr/bin/env python3
+"""Benchmark of the Direct-P FP4 attention forward on GB300.
+
+One step = the whole hot path on one batch of synthetic input already resident
+in HBM: NVFP4-quantize Q and K, MXFP4-quantize V, and the Direct-P forward.
+value = 4*B*H*N^2*D attention FLOPs per step / step time (TFLOP/s), summed
+over ranks (each rank runs its own replica of the workload: weak scaling).
+
+Default workload: B=1, H=40, N=32768, D=128 (video-DiT shape, token RMS
+spread), the largest configuration and the one the throughput target is
+quoted on.  Its inputs (1 GB bf16, 0.6 GB quantized) exceed the 129 MB L2, so
+no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain C restatement used by the
+tests) on a bounded sample of the same workload; it is a reported baseline.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Direct-P FP4 attn fwd TFLOP/s (4BHN²D/t), % of GB300 dense FP4 peak"
+UNIT = "TFLOP/s"
+# Dense FP4 : dense BF16 tensor throughput on GB300, nominal 13.5 : 2.25 PFLOP/s.
+FP4_OVER_BF16 = 13.5 / 2.25
+FALLBACK_BF16_TFLOPS = 1900.0
+
+# DRAM traffic of one forward launch, from an ncu capture (see profiles/), and
+# the hash of the kernel sources it was taken on; reported only while the
+# sources are unchanged.
+TRAFFIC_RECORD = {"sources_sha": None, "bytes_per_launch": None, "note": None}
+KERNEL_SOURCES = ["blackwell_nvfp4_quantize_gb300/csrc/fwd_directp.cu", "blackwell_nvfp4_quantize_gb300/csrc/ptx.cuh"]
+
+
+def sources_sha() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"bf16_tflops": FALLBACK_BF16_TFLOPS}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling over the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        loaded = [s for s in sm if smax and s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(w, q, k, v, budget_s=12.0):
+    """The oracle as it stands, on host cores, on a bounded row sample of head 0."""
+    import numpy as np
+
+    import oracle
+    from blackwell_nvfp4_quantize_gb300 import workloads as wl
+
+    threads = oracle.default_threads()
+    B, H, N, D = w.shape
+    head = slice(0, 1)
+    qb = wl.bf16_bits(q[:1, head].contiguous())
+    kb = wl.bf16_bits(k[:1, head].contiguous())
+    vb = wl.bf16_bits(v[:1, head].contiguous())
+    shape1 = (1, 1, N, D)
+    t0 = time.perf_counter()
+    qq = oracle.quant_nvfp4(qb, threads)
+    kq = oracle.quant_nvfp4(kb, threads)
+    vq = oracle.quant_mxfp4_v(vb, threads)
+    t_quant = time.perf_counter() - t0
+    # calibrate, then time a sample sized to the budget
+    probe = np.arange(min(N, 2 * threads), dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, probe, threads)
+    t_probe = time.perf_counter() - t0
+    rows = int(max(len(probe), min(N, len(probe) * budget_s / max(t_probe, 1e-6))))
+    sample = np.linspace(0, N - 1, rows).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, sample, threads)
+    t = time.perf_counter() - t0
+    flops = 4.0 * rows * N * D
+    return {"value": flops / t / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "%d of %d query rows of head 0 of %s (attention rows only; the oracle's quantization "
+                      "of that head took %.1f s and is excluded), %.1f s" % (rows, N, w.name, t_quant, t)}
+
+
+def run_reference(args, w):
+    """--impl reference: the CPU oracle on a bounded sample, per step."""
+    import numpy as np
+
+    import oracle
+    from blackwell_nvfp4_quantize_gb300 import workloads as wl
+
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    q, k, v = wl.make_inputs(w)
+    threads = oracle.default_threads()
+    B, H, N, D = w.shape
+    qb, kb, vb = (wl.bf16_bits(t[:1, :1].contiguous()) for t in (q, k, v))
+    shape1 = (1, 1, N, D)
+    qq, kq, vq = oracle.quant_nvfp4(qb, threads), oracle.quant_nvfp4(kb, threads), oracle.quant_mxfp4_v(vb, threads)
+    rows_per_step = max(threads, 2 * threads)
+    probe = np.arange(rows_per_step, dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, probe, threads)
+    t_probe = time.perf_counter() - t0
+    per_step_budget = max(0.5, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
+    rows_per_step = int(max(threads, min(N, rows_per_step * per_step_budget / max(t_probe, 1e-6))))
+    rng = np.random.default_rng(0)
+    times = []
+    for i in range(args.warmup + args.steps):
+        rows = np.sort(rng.choice(N, size=rows_per_step, replace=False)).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, rows, threads)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    t = sum(times)
+    flops = 4.0 * rows_per_step * N * D * len(times)
+    value = flops / t / 1e12
+    sample = "%d query rows per step of head 0 of %s (attention rows; quantization excluded)" % (rows_per_step, w.name)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * t / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "recipe": w.description},
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    import torch
+
+    import blackwell_nvfp4_quantize_gb300 as fa
+    from blackwell_nvfp4_quantize_gb300 import workloads as wl
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    B, H, N, D = w.shape
+
+    q_h, k_h, v_h = wl.make_inputs(w, seed=w.seed + rank)
+    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
+    qq, kq, vq = fa.empty_nvfp4(w.shape, dev), fa.empty_nvfp4(w.shape, dev), fa.empty_mxfp4(w.shape, dev)
+    o = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    launches_per_step = 3 + 3 + 1 + 1  # amax, quant, finalize (x2), V quant, forward
+
+    fwd_events = []
+
+    def step(record=False):
+        fa.quant_qk_nvfp4(q, out=qq, stream=stream)
+        fa.quant_qk_nvfp4(k, out=kq, stream=stream)
+        fa.quant_v_mxfp4(v, out=vq, stream=stream)
+        if record:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fa.fwd_directp(qq, kq, vq, w.softmax_scale, o=o, lse=lse, stream=stream)
+            e1.record(stream)
+            fwd_events.append((e0, e1))
+        else:
+            fa.fwd_directp(qq, kq, vq, w.softmax_scale, o=o, lse=lse, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if fa.device_status() != fa.FP4ATTN_OK:
+        raise RuntimeError("device-side wait timed out during warm-up")
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    with ClockSampler(local) as clocks:
+        barrier()
+        t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for _ in range(args.steps):
+            step(record=True)
+        t_stop.record(stream)
+        barrier()
+    ms_total = t_start.elapsed_time(t_stop)
+    fwd_ms = [a.elapsed_time(b) for a, b in fwd_events]
+    if fa.device_status() != fa.FP4ATTN_OK:
+        raise RuntimeError("device-side wait timed out in the timed region")
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    q_p, k_p, v_p = (t.pin_memory() for t in (q_h, k_h, v_h))
+    o_p = torch.empty((B, H, N, D), dtype=torch.bfloat16).pin_memory()
+    lse_p = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        q.copy_(q_p, non_blocking=True)
+        k.copy_(k_p, non_blocking=True)
+        v.copy_(v_p, non_blocking=True)
+        fa.quant_qk_nvfp4(q, out=qq, stream=stream)
+        fa.quant_qk_nvfp4(k, out=kq, stream=stream)
+        fa.quant_v_mxfp4(v, out=vq, stream=stream)
+        fa.fwd_directp(qq, kq, vq, w.softmax_scale, o=o, lse=lse, stream=stream)
+        o_p.copy_(o, non_blocking=True)
+        lse_p.copy_(lse, non_blocking=True)
+
+    e2e_steps = max(2, min(args.steps, 10))
+    e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    if dist is not None:
+        t = torch.tensor([ms_total, e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total, e2e_ms = float(t[0]), float(t[1])
+
+    flops = float(w.flops)
+    ms_step = ms_total / args.steps
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    fwd_avg = sum(fwd_ms) / len(fwd_ms)
+    achieved = flops / (fwd_avg * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS)) * FP4_OVER_BF16
+    traffic = TRAFFIC_RECORD["bytes_per_launch"] if TRAFFIC_RECORD["sources_sha"] == sources_sha() else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e2m1", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "H": H, "N": N, "D": D, "recipe": w.description,
+                   "step": "NVFP4 quantize Q and K, MXFP4 quantize V, Direct-P forward",
+                   "l2": "inputs larger than L2 (1 GB bf16 in, 0.6 GB quantized); no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "fwd_ms": fwd_avg,
+        "fwd_frac_of_fp4_peak": achieved / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": "%s bf16 dense x %.1f (nominal FP4:BF16 dense ratio), burst" % (peak_src, FP4_OVER_BF16),
+                     "kernel": "fwd_directp_kernel<128>"},
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": 3 * B * H * N * D * 2, "d2h_bytes_per_step": B * H * N * D * 2 + B * H * N * 4},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, q_h, k_h, v_h)
+    elif rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, q_h, k_h, v_h)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=4, help="workload index 1-5 (default 4)")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from blackwell_nvfp4_quantize_gb300 import workloads as wl
+
+    w = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

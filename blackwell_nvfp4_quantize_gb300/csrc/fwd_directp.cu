@@ -234,8 +234,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     int m_ref = 0;
     float l_run = 0.0f;
     bool ok = true;
+    // tcgen05.ld / tcgen05.st are warp-collective (.sync.aligned): every
+    // branch around them below is made warp-uniform with a vote.
     for (int j = 0; j < nkv; ++j) {
-      if (!(ok = mbar_wait(bar_s_full, j & 1, abort_flag, p.status, 20))) break;
+      ok = mbar_wait(bar_s_full, j & 1, abort_flag, p.status, 20);
+      if (!__all_sync(0xFFFFFFFFu, ok)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       float s[128];
       tmem_ld32(tS + 0, *reinterpret_cast<float(*)[32]>(s + 0));
@@ -299,12 +305,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (j > 0) {
         // the previous PV product must be done before P and O are touched
-        if (!(ok = mbar_wait(bar_o_full, (j - 1) & 1, abort_flag, p.status, 21))) break;
+        ok = mbar_wait(bar_o_full, (j - 1) & 1, abort_flag, p.status, 21);
+        if (!__all_sync(0xFFFFFFFFu, ok)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
       }
-      if (rescale) {
-        const float f = exp2_int(m_old - m_ref);
-        l_run *= f;
+      // Rescale O (and l) of the rows whose reference maximum moved; the whole
+      // warp takes part in the TMEM round trip, other rows multiply by 1.
+      const float f = rescale ? exp2_int(m_old - m_ref) : 1.0f;
+      l_run *= f;
+      if (__any_sync(0xFFFFFFFFu, rescale)) {
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           float o[32];
@@ -337,7 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar_p_full);
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && mbar_wait(bar_o_full, (nkv - 1) & 1, abort_flag, p.status, 22)) {
+    if (ok) ok = mbar_wait(bar_o_full, (nkv - 1) & 1, abort_flag, p.status, 22);
+    if (__all_sync(0xFFFFFFFFu, ok)) {
       tc_fence_after();
       const float inv_l = 1.0f / l_run;
       const bool store = qrow < N;
@@ -367,7 +380,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 5) {
+    __syncwarp();
+    tmem_dealloc(tmem, kTmemCols);
+  }
 }
 
 // ------------------------------------------------------------------ host side

@@ -19,6 +19,10 @@ pytestmark = pytest.mark.gpu
 O_TOL = 2e-2
 LSE_TOL = 1e-3
 CODE_AGREE = 0.999
+# O is stored in bf16 (round to nearest even: relative error <= 2^-9).  The
+# 2e-2 absolute bound is the one stated for the five workloads, whose outputs
+# stay of order one; edge cases with larger outputs add the bf16 rounding.
+BF16_REL = 2.0 ** -8
 
 
 def _quantize(q, k, v):
@@ -27,8 +31,9 @@ def _quantize(q, k, v):
     return fa.quant_qk_nvfp4(q.cuda()), fa.quant_qk_nvfp4(k.cuda()), fa.quant_v_mxfp4(v.cuda())
 
 
-def _run_and_check(q, k, v, scale, dump_slices, sample, label):
-    """dump_slices: list of (b, h, row0, nrows); sample: flat row ids for O/LSE."""
+def _run_and_check(q, k, v, scale, dump_slices, sample, label, o_rel=0.0):
+    """dump_slices: list of (b, h, row0, nrows); sample: flat row ids for O/LSE.
+    O must satisfy |dO| <= O_TOL + o_rel * |O_ref| elementwise."""
     import blackwell_nvfp4_quantize_gb300 as fa
 
     B, H, N, D = q.shape
@@ -42,7 +47,7 @@ def _run_and_check(q, k, v, scale, dump_slices, sample, label):
     assert np.all(np.isfinite(o_np)) and np.all(np.isfinite(lse_np))
     # O / LSE on sampled rows
     ref = oracle.directp_rows(qn, kn, vn, (B, H, N, D), scale, sample)
-    err_o = float(np.max(np.abs(o_np[sample] - ref["o"])))
+    err_o = float(np.max(np.abs(o_np[sample] - ref["o"]) - o_rel * np.abs(ref["o"])))
     err_l = float(np.max(np.abs(lse_np[sample] - ref["lse"])))
     # codes through the dump entry point (same kernel and launch shape)
     agree = total = kagree = ktotal = 0
@@ -108,7 +113,7 @@ def test_ragged_lengths(N, D):
     q, k, v = wl.make_custom(1, 2, N, D, seed=7 + N, kind="normal", scale=1.5)
     B, H = 1, 2
     _run_and_check(q, k, v, 1.0 / math.sqrt(D), [(0, 1, 0, N)], np.arange(B * H * N, dtype=np.int64),
-                   "ragged N=%d D=%d" % (N, D))
+                   "ragged N=%d D=%d" % (N, D), o_rel=BF16_REL)
 
 
 @pytest.mark.parametrize("D", [64, 128])
@@ -124,7 +129,7 @@ def test_large_scale_rows():
     # wide dynamic range of scores: many rescales of O, many zero codes
     q, k, v = wl.make_custom(1, 2, 640, 128, seed=12, kind="normal", scale=4.0)
     _run_and_check(q, k, v, 1.0 / math.sqrt(128), [(0, 0, 0, 640)], np.arange(2 * 640, dtype=np.int64),
-                   "scale 4")
+                   "scale 4", o_rel=BF16_REL)
 
 
 def test_timeout_status_word_is_clear():
