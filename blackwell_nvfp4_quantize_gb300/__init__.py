@@ -64,7 +64,7 @@ def lib():
     L.fp4attn_fwd_directp.argtypes = [ctypes.POINTER(_NVFP4), ctypes.POINTER(_NVFP4), ctypes.POINTER(_MXFP4),
                                       vp, vp, i, i, i, i, f, vp]
     L.fp4attn_debug_dump_p.argtypes = [ctypes.POINTER(_NVFP4), ctypes.POINTER(_NVFP4), ctypes.POINTER(_MXFP4),
-                                       vp, vp, i, i, i, i, f, i, i, i, i, vp, vp, vp]
+                                       vp, vp, i, i, i, i, f, i, i, i, i, vp, vp, vp, vp]
     L.fp4attn_device_status.argtypes = [vp]
     L.fp4attn_debug_cvt_transitions.argtypes = [i, ctypes.c_uint32, ctypes.c_uint32, vp, i, vp, vp]
     for name in ("fp4attn_debug_cvt_transitions", "fp4attn_nvfp4_bytes", "fp4attn_mxfp4_v_bytes", "fp4attn_quant_qk_nvfp4",
@@ -190,7 +190,8 @@ def fwd_directp(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP4Tensor, softmax_scale: f
 
 def debug_dump_p(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP4Tensor, b: int, h: int, row0: int, nrows: int,
                  softmax_scale: float | None = None, stream=None):
-    """fp4attn_debug_dump_p: (O, LSE, codes [nrows, Npad/2] u8, kshift [nrows, Npad/32] i32)."""
+    """fp4attn_debug_dump_p: (O, LSE, codes [nrows, Npad/2] u8, kshift [nrows, Npad/32] i32,
+    O of the dumped rows in fp32 [nrows, D])."""
     B, H, N, D = q.shape
     dev = q.payload.device
     if softmax_scale is None:
@@ -200,11 +201,13 @@ def debug_dump_p(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP4Tensor, b: int, h: int,
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     codes = torch.zeros((nrows, npad // 2), dtype=torch.uint8, device=dev)
     kshift = torch.zeros((nrows, npad // 32), dtype=torch.int32, device=dev)
+    o32 = torch.zeros((nrows, D), dtype=torch.float32, device=dev)
     qc, kc, vc = q._c(), k._c(), v._c()
     _check(lib().fp4attn_debug_dump_p(ctypes.byref(qc), ctypes.byref(kc), ctypes.byref(vc), _ptr(o), _ptr(lse),
                                       B, H, N, D, float(softmax_scale), b, h, row0, nrows, _ptr(codes),
-                                      _ptr(kshift), ctypes.c_void_p(_stream(stream))), "fp4attn_debug_dump_p")
-    return o, lse, codes, kshift
+                                      _ptr(kshift), _ptr(o32), ctypes.c_void_p(_stream(stream))),
+           "fp4attn_debug_dump_p")
+    return o, lse, codes, kshift, o32
 
 
 def device_status(stream=None) -> int:

@@ -83,6 +83,7 @@ struct FwdParams {
   int dump_bh, dump_row0, dump_nrows;
   uint8_t* dump_codes;
   int32_t* dump_kshift;
+  float* dump_o;  // fp32 O of the dumped rows, before the bf16 store
 };
 
 __device__ __forceinline__ float exp2_int(int e) {  // 2^e, e >= -149
@@ -372,6 +373,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 4; ++i)
             dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
         }
+        if (dump_row) {
+          float* od = p.dump_o + static_cast<size_t>(qrow - p.dump_row0) * D + 32 * cc;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) od[i] = o[i] * inv_l;
+        }
       }
       if (store) p.lse[static_cast<size_t>(bh) * N + qrow] = 0.69314718055994531f * (static_cast<float>(m_ref) + log2f(l_run));
     }
@@ -414,7 +420,7 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 template <int D, bool DUMP>
 int launch(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k, const fp4attn_mxfp4_t* v, void* o, float* lse,
            int B, int H, int N, float softmax_scale, int dump_bh, int row0, int nrows, uint8_t* codes,
-           int32_t* kshift, cudaStream_t stream) {
+           int32_t* kshift, float* o_f32, cudaStream_t stream) {
   using L = Layout<D>;
   DeviceStatus* status = device_status_ptr();
   if (!status) return FP4ATTN_ERR_CUDA;
@@ -450,6 +456,7 @@ int launch(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k, const fp4attn_mxf
   prm.dump_nrows = nrows;
   prm.dump_codes = codes;
   prm.dump_kshift = kshift;
+  prm.dump_o = o_f32;
   auto kern = fwd_directp_kernel<D, DUMP>;
   static std::once_flag attr_once[64];
   int dev = 0;
@@ -489,20 +496,21 @@ extern "C" int fp4attn_fwd_directp(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4
   const int st = check_fwd(q, k, v, o, lse, B, H, N, D, softmax_scale);
   if (st != FP4ATTN_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (D == 128) return launch<128, false>(q, k, v, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr, nullptr, s);
-  return launch<64, false>(q, k, v, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr, nullptr, s);
+  if (D == 128) return launch<128, false>(q, k, v, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr, nullptr, nullptr, s);
+  return launch<64, false>(q, k, v, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr, nullptr, nullptr, s);
 }
 
 extern "C" int fp4attn_debug_dump_p(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k, const fp4attn_mxfp4_t* v,
                                     void* o, float* lse, int B, int H, int N, int D, float softmax_scale, int b,
-                                    int h, int row0, int nrows, uint8_t* codes, int32_t* kshift, void* stream) {
+                                    int h, int row0, int nrows, uint8_t* codes, int32_t* kshift, float* o_f32,
+                                    void* stream) {
   const int st = check_fwd(q, k, v, o, lse, B, H, N, D, softmax_scale);
   if (st != FP4ATTN_OK) return st;
   if (b < 0 || b >= B || h < 0 || h >= H || row0 < 0 || nrows <= 0 || row0 + nrows > N || !codes || !kshift ||
-      !aligned16(codes) || !aligned16(kshift))
+      !o_f32 || !aligned16(codes) || !aligned16(kshift) || !aligned16(o_f32))
     return FP4ATTN_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int bh = b * H + h;
-  if (D == 128) return launch<128, true>(q, k, v, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes, kshift, s);
-  return launch<64, true>(q, k, v, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes, kshift, s);
+  if (D == 128) return launch<128, true>(q, k, v, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes, kshift, o_f32, s);
+  return launch<64, true>(q, k, v, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes, kshift, o_f32, s);
 }

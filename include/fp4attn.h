@@ -121,15 +121,16 @@ int fp4attn_fwd_directp(const fp4attn_nvfp4_t *q, const fp4attn_nvfp4_t *k, cons
                         void *stream);
 
 /* Same computation as fp4attn_fwd_directp (same kernel, same launch shape),
- * and in addition writes the probability codes and block shifts of query
- * rows row0 .. row0+nrows-1 of head (b, h):
+ * and in addition writes the probability codes, block shifts and fp32 output
+ * of query rows row0 .. row0+nrows-1 of head (b, h):
  *   codes:  [nrows, Npad/2] bytes, packed like the payloads (keys >= N are 0)
  *   kshift: [nrows, Npad/32] int32 block shifts K_b (0 for blocks past N)
+ *   o_f32:  [nrows, D] fp32, the normalised output before its bf16 rounding
  * For parity tests; O and LSE are written exactly as by the forward call. */
 int fp4attn_debug_dump_p(const fp4attn_nvfp4_t *q, const fp4attn_nvfp4_t *k, const fp4attn_mxfp4_t *v,
                          void *o, float *lse, int B, int H, int N, int D, float softmax_scale,
                          int b, int h, int row0, int nrows, uint8_t *codes, int32_t *kshift,
-                         void *stream);
+                         float *o_f32, void *stream);
 
 /* Test support (no counterpart in the method): for format 0 (E2M1) or 1
  * (E4M3), converts every fp32 bit pattern u in [lo, hi] with the hardware

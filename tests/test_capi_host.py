@@ -77,7 +77,7 @@ def test_argument_errors_without_gpu(L):
     bad = fa._NVFP4(0x1000, 0, 0x3000)
     assert L.fp4attn_fwd_directp(ctypes.byref(bad), ctypes.byref(q), ctypes.byref(v), good, good, 1, 1, 128, 64,
                                  ctypes.c_float(0.1), n) == fa.FP4ATTN_ERR_INVALID_ARG
-    assert L.fp4attn_debug_dump_p(*args, ctypes.c_float(0.1), 0, 0, 100, 64, good, good, n) == \
+    assert L.fp4attn_debug_dump_p(*args, ctypes.c_float(0.1), 0, 0, 100, 64, good, good, good, n) == \
         fa.FP4ATTN_ERR_INVALID_ARG  # rows beyond N
     assert L.fp4attn_fwd_directp(ctypes.byref(q), ctypes.byref(q), ctypes.byref(v), good, good, 300, 300, 128, 64,
                                  ctypes.c_float(0.1), n) == fa.FP4ATTN_ERR_UNSUPPORTED  # B*H > 65535
