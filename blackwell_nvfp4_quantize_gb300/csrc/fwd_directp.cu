@@ -6,19 +6,28 @@
 // conversion, denominator from the same rounded probabilities that PV
 // consumes, LSE saved with O).
 //
-// One CTA computes one 128-row query tile of one (b, h) and streams the key /
-// value tiles of that head through a TMA ring.  Roles (192 threads):
-//   warps 0-3  softmax: one thread per query row.  Reads its S row from TMEM,
-//              takes 32-key block maxima, maps scores to E2M1 codes
-//              (fp32 FMA + ex2 + hardware e2m1x2 conversion), sums the decoded
-//              codes for the denominator, writes the P tile and its E8M0
-//              scales to shared memory, rescales O in TMEM when the reference
-//              maximum moves, and finally normalises O and writes O / LSE.
-//   warp 4     TMA producer (one elected lane).
-//   warp 5     TMEM owner and single-thread tcgen05 MMA issuer:
-//              S = Q K^T  (kind::mxf4nvf4, 16-element UE4M3 scales)
-//              O += P V   (kind::mxf4, 32-element UE8M0 scales)
-// TMEM (512 columns): S [0,128), O [128,128+D), scale factors from 256 on.
+// One CTA computes two 128-row query tiles of one (b, h) and streams the key /
+// value tiles of that head through a TMA ring; both query tiles consume every
+// K/V tile.  Roles (352 threads):
+//   warps 0-3, 4-7  softmax warpgroups, one per query tile, one thread per
+//              query row.  Each reads its S row from TMEM (block maxima come
+//              out of tcgen05.ld.red), maps the scores to E2M1 codes (packed
+//              fp32 FMA, ex2, hardware e2m1x2 conversion), writes its P tile
+//              and E8M0 scale atom to shared memory, rescales its O
+//              accumulator when the reference maximum moves, and finally
+//              writes O and LSE.
+//   warp 8     TMA producer (one elected lane issues).
+//   warps 9,10 tcgen05 MMA issuers, one per query tile (one elected lane
+//              each; warp 9 also owns the TMEM allocation):
+//              S   = Q_t K^T     kind::mxf4nvf4, 16-element UE4M3 scales
+//              O_t += P_t V      kind::mxf4, 32-element UE8M0 scales
+//              l_t  = P_t 1      the same P operand against a tile of E2M1
+//                                ones: the tile's denominator from exactly the
+//                                codes and scales the PV product consumes; the
+//                                softmax warps add it up in fp32 registers
+// TMEM (512 columns): one score bank S shared by the two tiles (a softmax
+// warpgroup copies S to registers and releases the bank at once), two output
+// banks, two 16-column l banks, and the scale-factor columns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -31,40 +40,53 @@
 namespace fp4attn {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 352;
+constexpr int kWarpTma = 8, kWarpMma0 = 9;  // warps 9 and 10 issue the MMAs of query tiles 0 and 1
 constexpr int kStages = 3;
-// The MMA warp issues S(j+1) = Q K(j+1)^T before O += P(j) V(j), so the ring
-// must hold tiles j and j+1 at once.
+// The MMA warp of a tile issues S = Q K(j+1)^T before its PV product of tile
+// j, so the ring must hold tiles j and j+1 at once.
 static_assert(kStages >= 2, "the K/V ring needs at least two stages");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 128, kColSFQ = 256, kColSFK = 264, kColSFP = 272, kColSFV = 276;
+constexpr uint32_t kColS = 0;         // 128 columns: fp32 scores of 128 keys
+constexpr uint32_t kColO = 128;       // tile t output at kColO + t * D
+constexpr uint32_t kColL = 384;       // tile t denominator at kColL + 16 t
+constexpr uint32_t kColSFQ = 416;     // tile t Q scale atoms at kColSFQ + 8 t
+constexpr uint32_t kColSFK = 432;     // tile t, KV-step parity q: kColSFK + 16 t + 8 q
+constexpr uint32_t kColSFV = 464;     // tile t, KV-step parity q: kColSFV + 8 t + 4 q
+constexpr uint32_t kColSFP = 480;     // tile t P scale atom at kColSFP + 4 t
+constexpr uint32_t kColSFOnes = 488;  // tile t unit scales of the ones tile at kColSFOnes + 4 t
+static_assert(kColSFOnes + 8 <= kTmemCols, "TMEM plan exceeds 512 columns");
+constexpr uint32_t kLN = 16;                     // N of the denominator MMA
 constexpr float kLog2Six = 2.5849625007211561f;  // log2(6) rounded to fp32
 constexpr double kLog2E = 1.4426950408889634074;
-// The reference maximum M moves (and O is rescaled) only when a new tile's
-// ceil(max score) exceeds it by more than this many binades.
-constexpr int kRescaleSlack = 0;
+// The reference maximum M of a row moves (and O, l are rescaled by an exact
+// power of two) only when a tile's ceil(max score) exceeds it by more than
+// this many binades; until then probabilities may exceed 1 by up to 2^8.
+constexpr int kRescaleSlack = 8;
 
 template <int D>
 struct Layout {
   static constexpr int kRowBytes = D / 2;  // packed E2M1 bytes per Q/K row
-  static constexpr int kQ = 0;
   static constexpr int kTileQK = 128 * kRowBytes;
-  static constexpr int kTileV = D * 64;  // D channels x 128 keys
-  static constexpr int kK = kQ + kTileQK;
-  static constexpr int kV = kK + kStages * kTileQK;
-  static constexpr int kP = kV + kStages * kTileV;
-  static constexpr int kSFQ = kP + 128 * 64;
+  static constexpr int kTileV = D * 64;    // D channels x 128 keys
   static constexpr int kSFAtoms = D / 64;  // NVFP4 scale atoms per 128-row tile
-  static constexpr int kSFK = kSFQ + kSFAtoms * 512;
+  static constexpr int kQ = 0;             // two query tiles
+  static constexpr int kK = kQ + 2 * kTileQK;
+  static constexpr int kV = kK + kStages * kTileQK;
+  static constexpr int kP = kV + kStages * kTileV;  // two P tiles of 128 x 64 bytes
+  static constexpr int kOnes = kP + 2 * 8192;       // 16 rows x 64 bytes of E2M1 ones
+  static constexpr int kSFQ = kOnes + 1024;
+  static constexpr int kSFK = kSFQ + 2 * kSFAtoms * 512;
   static constexpr int kSFV = kSFK + kStages * kSFAtoms * 512;
   static constexpr int kSFP = kSFV + kStages * 512;
-  static constexpr int kBars = kSFP + 512;
-  static constexpr int kNumBars = 1 + 2 * kStages + 4;
+  static constexpr int kSFOnes = kSFP + 2 * 512;
+  static constexpr int kBars = kSFOnes + 512;
+  static constexpr int kNumBars = 1 + 2 * kStages + 8;  // q, kv full/empty, s_full/s_free/p_full/o_full x2
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   // Pad the request so that one CTA owns the SM: it allocates all 512 TMEM columns.
   static constexpr int kAlloc = (kBytes + 1024 > 120 * 1024) ? kBytes + 1024 : 120 * 1024;
-  static_assert(kTileQK % 1024 == 0 && kTileV % 1024 == 0, "tiles must keep 1024-B alignment");
+  static_assert(kTileQK % 1024 == 0 && kTileV % 1024 == 0 && kP % 1024 == 0, "tiles keep 1024-B alignment");
 };
 
 struct FwdParams {
@@ -92,14 +114,6 @@ __device__ __forceinline__ float exp2_int(int e) {  // 2^e, e >= -149
   return 0.0f;
 }
 
-// Sum of the decoded values of eight non-negative E2M1 codes, in units of 0.5,
-// as four byte lanes (each lane <= 24): a byte-permute table lookup.
-__device__ __forceinline__ uint32_t e2m1x8_halfsum_lanes(uint32_t w) {
-  constexpr uint32_t lo = 0x03020100u;  // 2 x {0, .5, 1, 1.5}
-  constexpr uint32_t hi = 0x0C080604u;  // 2 x {2, 3, 4, 6}
-  return __byte_perm(lo, hi, w & 0xFFFFu) + __byte_perm(lo, hi, w >> 16);
-}
-
 template <int D, bool DUMP>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_directp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -111,33 +125,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_q_full = bars;
   uint64_t* bar_kv_full = bars + 1;
   uint64_t* bar_kv_empty = bars + 1 + kStages;
-  uint64_t* bar_s_full = bars + 1 + 2 * kStages;
-  uint64_t* bar_s_free = bar_s_full + 1;
-  uint64_t* bar_p_full = bar_s_full + 2;
-  uint64_t* bar_o_full = bar_s_full + 3;
+  uint64_t* bar_s_full = bars + 1 + 2 * kStages;  // [2]
+  uint64_t* bar_s_free = bar_s_full + 2;          // [2]
+  uint64_t* bar_p_full = bar_s_full + 4;          // [2]
+  uint64_t* bar_o_full = bar_s_full + 6;          // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = blockIdx.x;
+  const int qt0 = 2 * blockIdx.x;  // first of the two query tiles
   const int bh = blockIdx.y;
   const int N = p.N;
   const int nkv = p.ntiles;
+  const bool has1 = (qt0 + 1) * 128 < N;  // the second query tile holds rows
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q_full, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_kv_full + s, 1);
-      mbar_init(bar_kv_empty + s, 1);
+      mbar_init(bar_kv_empty + s, has1 ? 2 : 1);  // one commit per MMA warp
     }
-    mbar_init(bar_s_full, 1);
-    mbar_init(bar_s_free, 128);
-    mbar_init(bar_p_full, 128);
-    mbar_init(bar_o_full, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar_s_full + t, 1);
+      mbar_init(bar_s_free + t, 4);  // one arrival per softmax warp
+      mbar_init(bar_p_full + t, 4);
+      mbar_init(bar_o_full + t, 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  // constant operands of the denominator MMA: E2M1 ones (0x22 = two 1.0 codes)
+  // and unit E8M0 scales (0x7F = 2^0)
+  for (int i = threadIdx.x; i < 1024 / 16; i += kThreads)
+    reinterpret_cast<uint4*>(smem + L::kOnes)[i] = make_uint4(0x22222222u, 0x22222222u, 0x22222222u, 0x22222222u);
+  for (int i = threadIdx.x; i < 512 / 16; i += kThreads)
+    reinterpret_cast<uint4*>(smem + L::kSFOnes)[i] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+  fence_proxy_async_smem();
+  if (warp == kWarpMma0) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -146,19 +170,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // The whole warp runs the loop and waits; one elected lane issues.
+    const bool leader = elect_one();
+    constexpr uint32_t kSfBytes = L::kSFAtoms * 512;
+    if (leader) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      constexpr uint32_t kSfBytes = L::kSFAtoms * 512;
-      mbar_arrive_expect_tx(bar_q_full, L::kTileQK + kSfBytes);
-      tma_load_3d(smem + L::kQ, &tm_q, bar_q_full, 0, qt * 128, bh);
-      bulk_load(smem + L::kSFQ, p.q_sf + (static_cast<size_t>(bh) * p.ntiles + qt) * kSfBytes, kSfBytes, bar_q_full);
-      for (int j = 0; j < nkv; ++j) {
-        const int s = j % kStages;
-        if (j >= kStages && !mbar_wait(bar_kv_empty + s, ((j / kStages) - 1) & 1, abort_flag, p.status, 1)) break;
+      mbar_arrive_expect_tx(bar_q_full, (has1 ? 2 : 1) * (L::kTileQK + kSfBytes));
+      for (int t = 0; t < (has1 ? 2 : 1); ++t) {
+        tma_load_3d(smem + L::kQ + t * L::kTileQK, &tm_q, bar_q_full, 0, (qt0 + t) * 128, bh);
+        bulk_load(smem + L::kSFQ + t * kSfBytes, p.q_sf + (static_cast<size_t>(bh) * p.ntiles + qt0 + t) * kSfBytes,
+                  kSfBytes, bar_q_full);
+      }
+    }
+    for (int j = 0; j < nkv; ++j) {
+      const int s = j % kStages;
+      if (j >= kStages) {
+        const bool ok = mbar_wait(bar_kv_empty + s, ((j / kStages) - 1) & 1, abort_flag, p.status, 1);
+        if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      }
+      if (leader) {
         mbar_arrive_expect_tx(bar_kv_full + s, L::kTileQK + L::kTileV + kSfBytes + 512);
         tma_load_3d(smem + L::kK + s * L::kTileQK, &tm_k, bar_kv_full + s, 0, j * 128, bh);
         tma_load_2d(smem + L::kV + s * L::kTileV, &tm_v, bar_kv_full + s, j * 64, bh * D);
@@ -167,97 +201,175 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_load(smem + L::kSFV + s * 512, p.v_sf + (static_cast<size_t>(bh) * p.ntiles + j) * 512, 512,
                   bar_kv_full + s);
       }
-      // Before leaving, make sure no copy into this CTA's shared memory is
-      // still in flight: wait for the last fill of every stage.
-      for (int j = nkv - kStages < 0 ? 0 : nkv - kStages; j < nkv; ++j)
-        mbar_wait(bar_kv_full + (j % kStages), (j / kStages) & 1, abort_flag, p.status, 2);
-      mbar_wait(bar_q_full, 0, abort_flag, p.status, 3);
+      __syncwarp();
     }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kSwizzleQK = (D == 128) ? 4u : 6u;  // 64-B or 32-B rows
-      constexpr uint32_t kSbo = 8 * L::kRowBytes;
-      constexpr uint32_t idesc_qk = idesc_fp4_block_scaled(128, 128, 0, 0, 0);
-      constexpr uint32_t idesc_pv0 = idesc_fp4_block_scaled(128, D, 1, 0, 0);
-      constexpr uint32_t idesc_pv1 = idesc_fp4_block_scaled(128, D, 1, 2, 2);
-      const uint64_t qdesc = smem_desc(smem_u32(smem + L::kQ), 16, kSbo, kSwizzleQK);
-      const uint64_t pdesc = smem_desc(smem_u32(smem + L::kP), 16, 512, 4);
-      bool ok = mbar_wait(bar_q_full, 0, abort_flag, p.status, 10);
-      if (ok) {
-        tc_fence_after();
-        for (int a = 0; a < L::kSFAtoms; ++a) tc_cp_sf_atom(tmem + kColSFQ + 4 * a, smem + L::kSFQ + a * 512);
-      }
-      auto issue_qk = [&](int j) {
-        const int s = j % kStages;
+    // Before leaving, make sure no copy into this CTA's shared memory is
+    // still in flight: wait for the last fill of every stage.
+    for (int j = nkv - kStages < 0 ? 0 : nkv - kStages; j < nkv; ++j)
+      mbar_wait(bar_kv_full + (j % kStages), (j / kStages) & 1, abort_flag, p.status, 2);
+    mbar_wait(bar_q_full, 0, abort_flag, p.status, 3);
+  } else if (warp == kWarpMma0 || (warp == kWarpMma0 + 1 && has1)) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 9 + t issues everything of query tile t.  The whole warp runs the
+    // loop and waits (so descriptors stay warp-uniform); one elected lane
+    // issues each group of tcgen05 operations.
+    const int t = warp - kWarpMma0;
+    const bool leader = elect_one();
+    constexpr uint32_t kSwizzleQK = (D == 128) ? 4u : 6u;  // 64-B or 32-B rows
+    constexpr uint32_t kSbo = 8 * L::kRowBytes;
+    constexpr uint32_t idesc_qk = idesc_fp4_block_scaled(128, 128, 0, 0, 0);
+    constexpr uint32_t idesc_pv0 = idesc_fp4_block_scaled(128, D, 1, 0, 0);
+    constexpr uint32_t idesc_pv1 = idesc_fp4_block_scaled(128, D, 1, 2, 2);
+    constexpr uint32_t idesc_l0 = idesc_fp4_block_scaled(128, kLN, 1, 0, 0);
+    constexpr uint32_t idesc_l1 = idesc_fp4_block_scaled(128, kLN, 1, 2, 2);
+    // Descriptors are built once; the start-address field is linear in the
+    // shared-memory address (16-byte units), so tiles are reached by adding
+    // their offset.
+    const uint64_t qdesc = smem_desc(smem_u32(smem + L::kQ + t * L::kTileQK), 16, kSbo, kSwizzleQK);
+    const uint64_t kdesc0 = smem_desc(smem_u32(smem + L::kK), 16, kSbo, kSwizzleQK);
+    const uint64_t vdesc0 = smem_desc(smem_u32(smem + L::kV), 16, 512, 4);
+    const uint64_t pdesc = smem_desc(smem_u32(smem + L::kP + t * 8192), 16, 512, 4);
+    const uint64_t ones_desc = smem_desc(smem_u32(smem + L::kOnes), 16, 512, 4);
+    constexpr uint64_t kQKStep = L::kTileQK >> 4, kVStep = L::kTileV >> 4;
+    const uint32_t t_s = tmem + kColS;
+    const uint32_t t_o = tmem + kColO + t * D;
+    const uint32_t t_l = tmem + kColL + 16 * t;
+    const uint32_t t_sfq = tmem + kColSFQ + 8 * t;
+    const uint32_t t_sfk = tmem + kColSFK + 16 * t;
+    const uint32_t t_sfv = tmem + kColSFV + 8 * t;
+    const uint32_t t_sfp = tmem + kColSFP + 4 * t;
+    const uint32_t t_sf1 = tmem + kColSFOnes + 4 * t;
+    uint64_t* s_full = bar_s_full + t;
+    uint64_t* p_full = bar_p_full + t;
+    uint64_t* o_full = bar_o_full + t;
+    auto wait = [&](uint64_t* bar, uint32_t parity, unsigned site) {
+      return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort_flag, p.status, site));
+    };
+    // The score bank is free for S_t(j) once the other tile has pulled its
+    // previous S into registers (tile 0, step j: tile 1's step j-1; tile 1,
+    // step j: tile 0's step j); without a second tile, once tile 0 has pulled
+    // its own previous S.
+    auto bank_free = [&](int j) {  // before S_t(j); j >= 1 for tile 0
+      if (t == 1) return wait(bar_s_free, j & 1, 12);
+      return wait(bar_s_free + (has1 ? 1 : 0), (j - 1) & 1, 13);
+    };
+    auto issue_qk = [&](int j) {  // K scale atoms of step j, then S = Q_t K(j)^T
+      const int s = j % kStages;
+      const uint32_t sfk = t_sfk + 8 * (j & 1);
+      if (leader) {
+#pragma unroll
         for (int a = 0; a < L::kSFAtoms; ++a)
-          tc_cp_sf_atom(tmem + kColSFK + 4 * a, smem + L::kSFK + (s * L::kSFAtoms + a) * 512);
-        const uint64_t kdesc = smem_desc(smem_u32(smem + L::kK + s * L::kTileQK), 16, kSbo, kSwizzleQK);
+          tc_cp_sf_atom(sfk + 4 * a, smem + L::kSFK + (s * L::kSFAtoms + a) * 512);
+#pragma unroll
         for (int ks = 0; ks < D / 64; ++ks)
-          mma_nvf4(tmem + kColS, qdesc + 2 * ks, kdesc + 2 * ks, idesc_qk, tmem + kColSFQ + 4 * ks,
-                   tmem + kColSFK + 4 * ks, ks > 0);
-        tc_commit(bar_s_full);
-      };
-      if (ok && (ok = mbar_wait(bar_kv_full, 0, abort_flag, p.status, 11))) {
-        tc_fence_after();
-        issue_qk(0);
+          mma_nvf4(t_s, qdesc + 2 * ks, kdesc0 + s * kQKStep + 2 * ks, idesc_qk, t_sfq + 4 * ks, sfk + 4 * ks,
+                   ks > 0);
+        tc_commit(s_full);
       }
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int s = j % kStages;
-        if (j + 1 < nkv) {
-          const int s1 = (j + 1) % kStages;
-          if (!(ok = mbar_wait(bar_kv_full + s1, ((j + 1) / kStages) & 1, abort_flag, p.status, 12))) break;
-          if (!(ok = mbar_wait(bar_s_free, j & 1, abort_flag, p.status, 13))) break;
-          tc_fence_after();
-          issue_qk(j + 1);
-        }
-        if (!(ok = mbar_wait(bar_p_full, j & 1, abort_flag, p.status, 14))) break;
-        tc_fence_after();
-        tc_cp_sf_atom(tmem + kColSFP, smem + L::kSFP);
-        tc_cp_sf_atom(tmem + kColSFV, smem + L::kSFV + s * 512);
-        const uint64_t vdesc = smem_desc(smem_u32(smem + L::kV + s * L::kTileV), 16, 512, 4);
-        mma_mxf4(tmem + kColO, pdesc, vdesc, idesc_pv0, tmem + kColSFP, tmem + kColSFV, j > 0);
-        mma_mxf4(tmem + kColO, pdesc + 2, vdesc + 2, idesc_pv1, tmem + kColSFP, tmem + kColSFV, true);
-        tc_commit(bar_o_full);
+      __syncwarp();
+    };
+    auto issue_pv = [&](int j) {  // P and V scale atoms, O_t += P_t V(j), l_t = P_t 1
+      const int s = j % kStages;
+      const uint32_t sfv = t_sfv + 4 * (j & 1);
+      const uint64_t vd = vdesc0 + s * kVStep;
+      if (leader) {
+        tc_cp_sf_atom(t_sfp, smem + L::kSFP + t * 512);
+        tc_cp_sf_atom(sfv, smem + L::kSFV + s * 512);
+        mma_mxf4(t_o, pdesc, vd, idesc_pv0, t_sfp, sfv, j > 0);
+        mma_mxf4(t_o, pdesc + 2, vd + 2, idesc_pv1, t_sfp, sfv, true);
+        mma_mxf4(t_l, pdesc, ones_desc, idesc_l0, t_sfp, t_sf1, false);
+        mma_mxf4(t_l, pdesc + 2, ones_desc + 2, idesc_l1, t_sfp, t_sf1, true);
+        tc_commit(o_full);
         tc_commit(bar_kv_empty + s);
       }
+      __syncwarp();
+    };
+
+    bool ok = wait(bar_q_full, 0, 10);
+    if (ok) {
+      tc_fence_after();
+      if (leader) {
+        for (int a = 0; a < L::kSFAtoms; ++a)
+          tc_cp_sf_atom(t_sfq + 4 * a, smem + L::kSFQ + (t * L::kSFAtoms + a) * 512);
+        tc_cp_sf_atom(t_sf1, smem + L::kSFOnes);
+      }
+      __syncwarp();
+      ok = wait(bar_kv_full, 0, 11);
     }
-  } else {
+    if (ok && t == 1) ok = wait(bar_s_free, 0, 12);  // tile 0 has pulled S_0(0)
+    if (ok) {
+      tc_fence_after();
+      issue_qk(0);
+    }
+    // Per KV step j: the next scores first (they need only K(j+1) and the
+    // bank), then this tile's PV product of step j.
+    for (int j = 0; ok && j < nkv; ++j) {
+      if (j + 1 < nkv) {
+        if (!(ok = wait(bar_kv_full + (j + 1) % kStages, ((j + 1) / kStages) & 1, 14))) break;
+        if (!(ok = bank_free(j + 1))) break;
+        tc_fence_after();
+        issue_qk(j + 1);
+      }
+      if (!(ok = wait(p_full, j & 1, 15))) break;
+      tc_fence_after();
+      issue_pv(j);
+    }
+  } else if (warp < 8 && (warp < 4 || has1)) {
     // ------------------------------------------------------------ softmax rows
-    const int row = threadIdx.x;  // 0..127 == TMEM lane
-    const int qrow = qt * 128 + row;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int t = warp >> 2;            // query tile of this warpgroup
+    const int row = threadIdx.x & 127;  // == TMEM lane
+    const int qrow = (qt0 + t) * 128 + row;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + kColS;
-    const uint32_t tO = tmem + lane_base + kColO;
+    const uint32_t tO = tmem + lane_base + kColO + t * D;
+    const uint32_t tL = tmem + lane_base + kColL + 16 * t;
+    uint64_t* s_full = bar_s_full + t;
+    uint64_t* s_free = bar_s_free + t;
+    uint64_t* p_full = bar_p_full + t;
+    uint64_t* o_full = bar_o_full + t;
+    uint8_t* sP = smem + L::kP + t * 8192;
+    uint8_t* sSFP = smem + L::kSFP + t * 512;
     const float c = static_cast<float>(((static_cast<double>(p.softmax_scale) * kLog2E) *
                                         static_cast<double>(*p.g_q)) * static_cast<double>(*p.g_k));
     const bool dump_row = DUMP && bh == p.dump_bh && qrow >= p.dump_row0 && qrow < p.dump_row0 + p.dump_nrows;
     int m_ref = 0;
-    float l_run = 0.0f;
+    float l_run = 0.0f;  // denominator, relative to 2^m_ref
     bool ok = true;
     // tcgen05.ld / tcgen05.st are warp-collective (.sync.aligned): every
     // branch around them below is made warp-uniform with a vote.
     for (int j = 0; j < nkv; ++j) {
-      ok = mbar_wait(bar_s_full, j & 1, abort_flag, p.status, 20);
+      ok = mbar_wait(s_full, j & 1, abort_flag, p.status, 20);
       if (!__all_sync(0xFFFFFFFFu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      // S row and its 32-key block maxima, reduced while leaving TMEM; the
+      // bank goes back to the MMA warps as soon as the row is in registers.
       float s[128];
-      tmem_ld32(tS + 0, *reinterpret_cast<float(*)[32]>(s + 0));
-      tmem_ld32(tS + 32, *reinterpret_cast<float(*)[32]>(s + 32));
-      tmem_ld32(tS + 64, *reinterpret_cast<float(*)[32]>(s + 64));
-      tmem_ld32(tS + 96, *reinterpret_cast<float(*)[32]>(s + 96));
+      float bm[4];
+      bm[0] = tmem_ld32_max(tS + 0, *reinterpret_cast<float(*)[32]>(s + 0));
+      bm[1] = tmem_ld32_max(tS + 32, *reinterpret_cast<float(*)[32]>(s + 32));
+      bm[2] = tmem_ld32_max(tS + 64, *reinterpret_cast<float(*)[32]>(s + 64));
+      bm[3] = tmem_ld32_max(tS + 96, *reinterpret_cast<float(*)[32]>(s + 96));
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(bar_s_free);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free);
 
       const int valid = N - j * 128;  // keys of this tile that exist (>= 1)
       if (valid < 128) {
+        // partial last tile: keys past N are masked and the maxima retaken
 #pragma unroll
         for (int i = 0; i < 128; ++i)
           if (i >= valid) s[i] = -INFINITY;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          float m = fmax3(s[32 * b], s[32 * b + 1], s[32 * b + 2]);
+#pragma unroll
+          for (int i = 3; i < 31; i += 2) m = fmax3(m, s[32 * b + i], s[32 * b + i + 1]);
+          bm[b] = fmaxf(m, s[32 * b + 31]);
+        }
       }
       // block maxima of the scaled scores (c > 0, so max(c*s) = c*max(s))
       float xb[4];
@@ -265,15 +377,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       float xmax = -INFINITY;
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        float m = s[32 * b];
-#pragma unroll
-        for (int i = 1; i < 32; ++i) m = fmaxf(m, s[32 * b + i]);
-        xb[b] = __fmul_rn(c, m);
+        xb[b] = __fmul_rn(c, bm[b]);
         xmax = fmaxf(xmax, xb[b]);
         kb[b] = (xb[b] == -INFINITY) ? 0 : static_cast<int>(ceilf(__fsub_rn(xb[b], kLog2Six)));
       }
       const int m_tile = static_cast<int>(ceilf(xmax));
-      int m_old = m_ref;
+      const int m_old = m_ref;
       bool rescale = false;
       if (j == 0) {
         m_ref = m_tile;
@@ -281,43 +390,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_ref = m_tile;
         rescale = true;
       }
-      // Direct-P: codes of 2^(X - K_b), packed 8 per word
+      // Direct-P: codes of 2^(X - K_b) = 2^(c*s - K_b), eight per word
       uint32_t w[16];
-      float l_tile = 0.0f;
       uint32_t sfword = 0;
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
         const float nk = static_cast<float>(-kb[b]);
-        uint32_t lanes = 0;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          float y[8];
+          const float* sv = s + 32 * b + 8 * q;
+          float x[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) y[i] = ex2_approx(__fmaf_rn(c, s[32 * b + 8 * q + i], nk));
-          w[4 * b + q] = cvt_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
-          lanes += e2m1x8_halfsum_lanes(w[4 * b + q]);
+          for (int i = 0; i < 8; i += 2) ffma2(x[i], x[i + 1], c, c, sv[i], sv[i + 1], nk, nk);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[i] = ex2_approx(x[i]);
+          w[4 * b + q] = cvt_e2m1x8(x[0], x[1], x[2], x[3], x[4], x[5], x[6], x[7]);
         }
-        const int halfsum = __dp4a(static_cast<int>(lanes), 0x01010101, 0);
         int e = kb[b] - m_ref;
         e = e < -127 ? -127 : e;
         const uint32_t byte = (xb[b] == -INFINITY) ? 0u : static_cast<uint32_t>(e + 127);
         sfword |= byte << (8 * b);
-        l_tile += static_cast<float>(halfsum) * exp2_int(e - 1);
       }
+      // The previous PV product must be done before this tile's P buffer and
+      // the O / l banks are touched; it normally finished long ago.  Its tile
+      // denominator (relative to the reference it was made with) joins l.
+      float l_prev = 0.0f;
       if (j > 0) {
-        // the previous PV product must be done before P and O are touched
-        ok = mbar_wait(bar_o_full, (j - 1) & 1, abort_flag, p.status, 21);
+        ok = mbar_wait(o_full, (j - 1) & 1, abort_flag, p.status, 21);
         if (!__all_sync(0xFFFFFFFFu, ok)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        l_prev = tmem_ld1(tL);  // completes at a wait below
       }
-      // Rescale O (and l) of the rows whose reference maximum moved; the whole
-      // warp takes part in the TMEM round trip, other rows multiply by 1.
-      const float f = rescale ? exp2_int(m_old - m_ref) : 1.0f;
-      l_run *= f;
+      // Rescale O of the rows whose reference maximum moved; the whole warp
+      // takes part in the TMEM round trip, other rows multiply by 1.
       if (__any_sync(0xFFFFFFFFu, rescale)) {
+        tmem_wait_ld();
+        l_run += l_prev;
+        l_prev = 0.0f;
+        const float f = rescale ? exp2_int(m_old - m_ref) : 1.0f;
+        l_run *= f;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           float o[32];
@@ -329,14 +443,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
       }
-      l_run += l_tile;
-      uint8_t* prow = smem + L::kP + row * 64;
+      uint8_t* prow = sP + row * 64;
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
         const int chunk = b ^ ((row >> 1) & 3);  // 64-byte swizzle of the K-major P tile
         *reinterpret_cast<uint4*>(prow + chunk * 16) = make_uint4(w[4 * b], w[4 * b + 1], w[4 * b + 2], w[4 * b + 3]);
       }
-      *reinterpret_cast<uint32_t*>(smem + L::kSFP + (row & 31) * 16 + (row >> 5) * 4) = sfword;
+      *reinterpret_cast<uint32_t*>(sSFP + (row & 31) * 16 + (row >> 5) * 4) = sfword;
       if (dump_row) {
         const size_t rr = static_cast<size_t>(qrow - p.dump_row0);
         uint4* dst = reinterpret_cast<uint4*>(p.dump_codes + rr * (p.ntiles * 64) + j * 64);
@@ -345,15 +458,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int b = 0; b < 4; ++b) p.dump_kshift[rr * (p.ntiles * 4) + j * 4 + b] = kb[b];
       }
+      tmem_wait_ld();
+      l_run += l_prev;
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar_p_full);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
     }
     // ------------------------------------------------------------ epilogue
-    if (ok) ok = mbar_wait(bar_o_full, (nkv - 1) & 1, abort_flag, p.status, 22);
+    if (ok) ok = mbar_wait(o_full, (nkv - 1) & 1, abort_flag, p.status, 22);
     if (__all_sync(0xFFFFFFFFu, ok)) {
       tc_fence_after();
-      const float inv_l = 1.0f / l_run;
+      const float l = l_run + tmem_ld1(tL);
+      tmem_wait_ld();
+      const float inv_l = 1.0f / l;
       const bool store = qrow < N;
       __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * N + (store ? qrow : 0)) * D;
 #pragma unroll
@@ -361,11 +479,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         float o[32];
         tmem_ld32(tO + 32 * cc, o);
         tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] *= inv_l;
         if (store) {
           uint32_t packed[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(o[2 * i] * inv_l, o[2 * i + 1] * inv_l);
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
             packed[i] = *reinterpret_cast<uint32_t*>(&h2);
           }
           uint4* dst = reinterpret_cast<uint4*>(orow + 32 * cc);
@@ -376,17 +496,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (dump_row) {
           float* od = p.dump_o + static_cast<size_t>(qrow - p.dump_row0) * D + 32 * cc;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) od[i] = o[i] * inv_l;
+          for (int i = 0; i < 32; ++i) od[i] = o[i];
         }
       }
-      if (store) p.lse[static_cast<size_t>(bh) * N + qrow] = 0.69314718055994531f * (static_cast<float>(m_ref) + log2f(l_run));
+      if (store)
+        p.lse[static_cast<size_t>(bh) * N + qrow] = 0.69314718055994531f * (static_cast<float>(m_ref) + log2f(l));
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) {
+  if (warp == kWarpMma0) {
     __syncwarp();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -466,7 +587,7 @@ int launch(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k, const fp4attn_mxf
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   });
   if (attr_err != cudaSuccess) return FP4ATTN_ERR_CUDA;
-  dim3 grid(ntiles, BH);
+  dim3 grid((ntiles + 1) / 2, BH);
   kern<<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, prm);
   return cuda_status(cudaGetLastError());
 }

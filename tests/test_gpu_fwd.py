@@ -120,7 +120,7 @@ def test_ragged_lengths(N, D):
     q, k, v = wl.make_custom(1, 2, N, D, seed=7 + N, kind="normal", scale=1.5)
     B, H = 1, 2
     _run_and_check(q, k, v, 1.0 / math.sqrt(D), [(0, 1, 0, N)], np.arange(B * H * N, dtype=np.int64),
-                   "ragged N=%d D=%d" % (N, D), o_rel=BF16_REL)
+                   "ragged N=%d D=%d" % (N, D))
 
 
 @pytest.mark.parametrize("D", [64, 128])
