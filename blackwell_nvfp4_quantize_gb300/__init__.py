@@ -66,8 +66,10 @@ def lib():
     L.fp4attn_debug_dump_p.argtypes = [ctypes.POINTER(_NVFP4), ctypes.POINTER(_NVFP4), ctypes.POINTER(_MXFP4),
                                        vp, vp, i, i, i, i, f, i, i, i, i, vp, vp, vp, vp]
     L.fp4attn_device_status.argtypes = [vp]
+    L.fp4attn_fwd_directp_noalloc.argtypes = [ctypes.POINTER(_NVFP4), ctypes.POINTER(_NVFP4),
+                                              ctypes.POINTER(_MXFP4), vp, vp, i, i, i, i, f, vp]
     L.fp4attn_debug_cvt_transitions.argtypes = [i, ctypes.c_uint32, ctypes.c_uint32, vp, i, vp, vp]
-    for name in ("fp4attn_debug_cvt_transitions", "fp4attn_nvfp4_bytes", "fp4attn_mxfp4_v_bytes", "fp4attn_quant_qk_nvfp4",
+    for name in ("fp4attn_fwd_directp_noalloc", "fp4attn_debug_cvt_transitions", "fp4attn_nvfp4_bytes", "fp4attn_mxfp4_v_bytes", "fp4attn_quant_qk_nvfp4",
                  "fp4attn_quant_v_mxfp4", "fp4attn_fwd_directp", "fp4attn_debug_dump_p",
                  "fp4attn_device_status"):
         getattr(L, name).restype = i
@@ -185,6 +187,21 @@ def fwd_directp(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP4Tensor, softmax_scale: f
     _check(lib().fp4attn_fwd_directp(ctypes.byref(qc), ctypes.byref(kc), ctypes.byref(vc), _ptr(o), _ptr(lse),
                                      B, H, N, D, float(softmax_scale), ctypes.c_void_p(_stream(stream))),
            "fp4attn_fwd_directp")
+    return o, lse
+
+
+def fwd_directp_noalloc(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP4Tensor, o: torch.Tensor, lse: torch.Tensor,
+                        softmax_scale: float | None = None, stream=None):
+    """fp4attn_fwd_directp_noalloc: the same forward with no device allocation
+    anywhere on its path; the caller provides O and LSE.  A bounded wait that
+    gives up shows as NaN in every LSE entry instead of a status code."""
+    B, H, N, D = q.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    qc, kc, vc = q._c(), k._c(), v._c()
+    _check(lib().fp4attn_fwd_directp_noalloc(ctypes.byref(qc), ctypes.byref(kc), ctypes.byref(vc), _ptr(o),
+                                             _ptr(lse), B, H, N, D, float(softmax_scale),
+                                             ctypes.c_void_p(_stream(stream))), "fp4attn_fwd_directp_noalloc")
     return o, lse
 
 

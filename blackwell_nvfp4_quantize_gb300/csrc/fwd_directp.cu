@@ -541,9 +541,9 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 template <int D, bool DUMP>
 int launch(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k, const fp4attn_mxfp4_t* v, void* o, float* lse,
            int B, int H, int N, float softmax_scale, int dump_bh, int row0, int nrows, uint8_t* codes,
-           int32_t* kshift, float* o_f32, cudaStream_t stream) {
+           int32_t* kshift, float* o_f32, cudaStream_t stream, DeviceStatus* status_word = nullptr) {
   using L = Layout<D>;
-  DeviceStatus* status = device_status_ptr();
+  DeviceStatus* status = status_word ? status_word : device_status_ptr();
   if (!status) return FP4ATTN_ERR_CUDA;
   const int ntiles = n_row_tiles(N);
   const int BH = B * H;
@@ -634,4 +634,70 @@ extern "C" int fp4attn_debug_dump_p(const fp4attn_nvfp4_t* q, const fp4attn_nvfp
   const int bh = b * H + h;
   if (D == 128) return launch<128, true>(q, k, v, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes, kshift, o_f32, s);
   return launch<64, true>(q, k, v, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes, kshift, o_f32, s);
+}
+
+// ------------------------------------------------------------------ allocation-free variant
+// fp4attn_fwd_directp_noalloc runs the same kernel, but the one piece of
+// memory the forward uses beyond its inputs and outputs -- the status word its
+// bounded waits report into, normally a block the library cudaMallocs on the
+// first call on each device -- lives in the static device array below, which
+// exists on every GPU that loads the library for as long as the process runs.
+namespace fp4attn {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 256;  // the array's size; each call uses sizeof(DeviceStatus)
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+DeviceStatus* g_noalloc_status[64] = {};
+
+// Device address of the static scratch on the current device.  The name of a
+// __device__ array means nothing to the host, so its address is looked up
+// once per device (with that device current) and cached.
+DeviceStatus* noalloc_status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_status[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return nullptr;
+    g_noalloc_status[dev] = static_cast<DeviceStatus*>(ptr);
+  }
+  return g_noalloc_status[dev];
+}
+
+// A caller of the allocation-free entry point has no status word to read, so
+// a bounded wait that gave up is made visible in the outputs: every LSE entry
+// becomes NaN.  Without a timeout each thread reads one word and returns.
+__global__ void noalloc_report_timeout(const DeviceStatus* status, float* lse, long long n) {
+  if (status->timeout == 0u) return;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    lse[i] = __int_as_float(0x7FC00000);
+}
+
+}  // namespace
+}  // namespace fp4attn
+
+extern "C" int fp4attn_fwd_directp_noalloc(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k,
+                                           const fp4attn_mxfp4_t* v, void* o, float* lse, int B, int H, int N, int D,
+                                           float softmax_scale, void* stream) {
+  const int st = check_fwd(q, k, v, o, lse, B, H, N, D, softmax_scale);
+  if (st != FP4ATTN_OK) return st;
+  // The scratch this call needs does not grow with the problem: one status
+  // word for any supported size.  Anything that needed more would be refused.
+  if (sizeof(DeviceStatus) > kNoAllocScratchBytes) return FP4ATTN_ERR_UNSUPPORTED;
+  DeviceStatus* status = noalloc_status_word();
+  if (!status) return FP4ATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the array keeps the previous call's contents: clear the word first
+  if (cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s) != cudaSuccess) return FP4ATTN_ERR_CUDA;
+  const int r = (D == 128)
+                    ? launch<128, false>(q, k, v, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr, nullptr, nullptr, s,
+                                         status)
+                    : launch<64, false>(q, k, v, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr, nullptr, nullptr, s,
+                                        status);
+  if (r != FP4ATTN_OK) return r;
+  noalloc_report_timeout<<<sm_count(), 256, 0, s>>>(status, lse, static_cast<long long>(B) * H * N);
+  return cuda_status(cudaGetLastError());
 }

@@ -120,6 +120,32 @@ int fp4attn_fwd_directp(const fp4attn_nvfp4_t *q, const fp4attn_nvfp4_t *k, cons
                         void *o, float *lse, int B, int H, int N, int D, float softmax_scale,
                         void *stream);
 
+/* Allocation-free variant of fp4attn_fwd_directp (the paper has no
+ * counterpart; this is an interface convenience).  Some callers cannot let a
+ * library call cudaMalloc: processes that have reserved almost all device
+ * memory up front for their own pool (a late allocation fails or fragments
+ * it), frameworks that route every device allocation through their own
+ * allocator and forbid side allocations, and latency-critical loops where an
+ * allocation's implicit device synchronisation is unacceptable.  This entry
+ * point computes exactly what fp4attn_fwd_directp computes, with the same
+ * arguments, layouts and errors, and never calls cudaMalloc, cudaFree or any
+ * allocating routine.  The only memory the forward needs besides the caller's
+ * inputs and outputs is its status word (8 bytes, for any problem size); here
+ * it lives in a static 256-byte device array that every GPU loading the
+ * library holds until the process exits.
+ *   - The first call on each device looks up that array's device address
+ *     (cudaGetSymbolAddress, with the device current) and caches it; make that
+ *     first call before any stream capture begins.
+ *   - Every call clears the word on `stream` before launching.  All calls share
+ *     the one array, so calls whose work overlaps on the GPU (for example on
+ *     two streams) race on it.
+ *   - There is no status word to read back: if a bounded device-side wait
+ *     gives up, every LSE entry of that call is set to NaN (O is incomplete).
+ * Launches a memset, the forward kernel and a small check kernel on stream. */
+int fp4attn_fwd_directp_noalloc(const fp4attn_nvfp4_t *q, const fp4attn_nvfp4_t *k, const fp4attn_mxfp4_t *v,
+                                void *o, float *lse, int B, int H, int N, int D, float softmax_scale,
+                                void *stream);
+
 /* Same computation as fp4attn_fwd_directp (same kernel, same launch shape),
  * and in addition writes the probability codes, block shifts and fp32 output
  * of query rows row0 .. row0+nrows-1 of head (b, h):
