@@ -17,10 +17,9 @@
 //              accumulator when the reference maximum moves, and finally
 //              writes O and LSE.  The score bank S is shared by the two
 //              tiles: as soon as all four warps of a warpgroup hold their S
-//              rows in registers (one mbarrier arrival per warp), one of its
-//              threads issues the next S = Q K^T into the bank (for the other
-//              tile), so the bank changes hands without a round trip through
-//              another warp.
+//              rows in registers, the last of its warps to get there issues
+//              the next S = Q K^T into the bank (for the other tile), so the
+//              bank changes hands without a round trip through another warp.
 //   warp 8     TMA producer (one elected lane issues).
 //   warps 9,10 PV issuers, one per query tile (one elected lane each; warp
 //              9 also owns the TMEM allocation and issues the first S):
@@ -85,7 +84,7 @@ struct Layout {
   static constexpr int kSFP = kSFV + kStages * 512;
   static constexpr int kSFOnes = kSFP + 2 * 512;
   static constexpr int kBars = kSFOnes + 512;
-  static constexpr int kNumBars = 1 + 2 * kStages + 8;  // q, kv full/empty, s_full/s_free/p_full/o_full x2
+  static constexpr int kNumBars = 1 + 2 * kStages + 6;  // q, kv full/empty, s_full/p_full/o_full x2
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   // Pad the request so that one CTA owns the SM: it allocates all 512 TMEM columns.
@@ -152,11 +151,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_kv_full = bars + 1;
   uint64_t* bar_kv_empty = bars + 1 + kStages;
   uint64_t* bar_s_full = bars + 1 + 2 * kStages;  // [2]
-  uint64_t* bar_s_free = bar_s_full + 2;          // [2]
-  uint64_t* bar_p_full = bar_s_full + 4;          // [2]
-  uint64_t* bar_o_full = bar_s_full + 6;          // [2]
+  uint64_t* bar_p_full = bar_s_full + 2;          // [2]
+  uint64_t* bar_o_full = bar_s_full + 4;          // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  uint32_t* s_loaded = reinterpret_cast<uint32_t*>(smem + L::kMisc + 8);  // [2] warps that hold their S rows
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qt0 = 2 * blockIdx.x;  // first of the two query tiles
@@ -173,8 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar_s_full + t, 1);
-      mbar_init(bar_s_free + t, 4);  // one arrival per softmax warp
-      mbar_init(bar_p_full + t, 4);
+      mbar_init(bar_p_full + t, 4);  // one arrival per softmax warp
+      s_loaded[t] = 0;
       mbar_init(bar_o_full + t, 1);
     }
     *abort_flag = 0;
@@ -309,7 +308,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + lane_base + kColO + t * D;
     const uint32_t tL = tmem + lane_base + kColL + 16 * t;
     uint64_t* s_full = bar_s_full + t;
-    uint64_t* s_free = bar_s_free + t;
     uint64_t* p_full = bar_p_full + t;
     uint64_t* o_full = bar_o_full + t;
     uint8_t* sP = smem + L::kP + t * 8192;
@@ -338,25 +336,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       bm[2] = tmem_ld32_max(tS + 64, *reinterpret_cast<float(*)[32]>(s + 64));
       bm[3] = tmem_ld32_max(tS + 96, *reinterpret_cast<float(*)[32]>(s + 96));
       tmem_wait_ld();
-      // Once all four warps hold their rows, the bank is free: one thread of
-      // this warpgroup issues the next S into it -- for the other tile at the
-      // same step (tile 0 -> tile 1) or the next step (tile 1 -> tile 0), or
-      // for this tile's next step when there is no second tile.  The other
-      // warps only arrive; the issuing thread's waits are bounded.
+      // Once all four warps hold their rows, the bank is free.  Each warp
+      // counts itself in; the last of the four issues the next S into the
+      // bank -- for the other tile at the same step (tile 0 -> tile 1) or the
+      // next step (tile 1 -> tile 0), or for this tile's next step when there
+      // is no second tile.  Nobody waits for anybody here.
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(s_free);
-      {
+      if (lane == 0 && (smem_atomic_add_acq_rel(s_loaded + t, 1u) & 3u) == 3u) {
         const int u = has1 ? 1 - t : 0;
         const int jn = (has1 && t == 0) ? j : j + 1;
-        if (row == 0 && jn < nkv) {
-          if (mbar_wait(s_free, j & 1, abort_flag, p.status, 23) &&
-              mbar_wait(bar_kv_full + jn % kStages, (jn / kStages) & 1, abort_flag, p.status, 24)) {
-            tc_fence_after();
-            issue_qk<D>(smem, tmem, u, jn, bar_s_full + u);
-          }
+        if (jn < nkv && mbar_wait(bar_kv_full + jn % kStages, (jn / kStages) & 1, abort_flag, p.status, 23)) {
+          tc_fence_after();
+          issue_qk<D>(smem, tmem, u, jn, bar_s_full + u);
         }
       }
+      __syncwarp();
 
       const int valid = N - j * 128;  // keys of this tile that exist (>= 1)
       if (valid < 128) {

@@ -85,6 +85,15 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
+// Shared-memory counter increment with acquire-release ordering at CTA
+// scope; returns the previous value.
+__device__ __forceinline__ uint32_t smem_atomic_add_acq_rel(uint32_t* addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_u32(addr)), "r"(v)
+               : "memory");
+  return old;
+}
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
