@@ -15,22 +15,19 @@
 //              fp32 FMA, ex2, hardware e2m1x2 conversion), writes its P tile
 //              and E8M0 scale atom to shared memory, rescales its O
 //              accumulator when the reference maximum moves, and finally
-//              writes O and LSE.  The score bank S is shared by the two
-//              tiles: as soon as all four warps of a warpgroup hold their S
-//              rows in registers, the last of its warps to get there issues
-//              the next S = Q K^T into the bank (for the other tile), so the
-//              bank changes hands without a round trip through another warp.
+//              writes O and LSE.
 //   warp 8     TMA producer (one elected lane issues).
-//   warps 9,10 PV issuers, one per query tile (one elected lane each; warp
-//              9 also owns the TMEM allocation and issues the first S):
+//   warps 9,10 tcgen05 MMA issuers, one per query tile (one elected lane
+//              each; warp 9 also owns the TMEM allocation):
+//              S   = Q_t K^T     kind::mxf4nvf4, 16-element UE4M3 scales
 //              O_t += P_t V      kind::mxf4, 32-element UE8M0 scales
 //              l_t  = P_t 1      the same P operand against a tile of E2M1
 //                                ones: the tile's denominator from exactly the
 //                                codes and scales the PV product consumes; the
 //                                softmax warps add it up in fp32 registers
-//   S products: kind::mxf4nvf4 with 16-element UE4M3 scales.
-// TMEM (512 columns): the score bank, two output banks, two 16-column l
-// banks, and the scale-factor columns.
+// TMEM (512 columns): one score bank S shared by the two tiles (a softmax
+// warpgroup copies S to registers and releases the bank at once), two output
+// banks, two 16-column l banks, and the scale-factor columns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -44,10 +41,10 @@ namespace fp4attn {
 namespace {
 
 constexpr int kThreads = 352;
-constexpr int kWarpTma = 8, kWarpMma0 = 9;  // warps 9 and 10 issue the PV products of query tiles 0 and 1
+constexpr int kWarpTma = 8, kWarpMma0 = 9;  // warps 9 and 10 issue the MMAs of query tiles 0 and 1
 constexpr int kStages = 3;
-// S = Q K(j+1)^T is issued while PV of tile j is still pending, so the ring
-// must hold tiles j and j+1 at once.
+// The MMA warp of a tile issues S = Q K(j+1)^T before its PV product of tile
+// j, so the ring must hold tiles j and j+1 at once.
 static_assert(kStages >= 2, "the K/V ring needs at least two stages");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;         // 128 columns: fp32 scores of 128 keys
@@ -84,7 +81,7 @@ struct Layout {
   static constexpr int kSFP = kSFV + kStages * 512;
   static constexpr int kSFOnes = kSFP + 2 * 512;
   static constexpr int kBars = kSFOnes + 512;
-  static constexpr int kNumBars = 1 + 2 * kStages + 6;  // q, kv full/empty, s_full/p_full/o_full x2
+  static constexpr int kNumBars = 1 + 2 * kStages + 8;  // q, kv full/empty, s_full/s_free/p_full/o_full x2
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   // Pad the request so that one CTA owns the SM: it allocates all 512 TMEM columns.
@@ -117,28 +114,6 @@ __device__ __forceinline__ float exp2_int(int e) {  // 2^e, e >= -149
   return 0.0f;
 }
 
-// S = Q_u K(j)^T for query tile u into the score bank, by the calling thread:
-// the K scale atoms of step j go to tile u's TMEM columns for that step's
-// parity, then the block-scaled MMAs, then a commit to u's s_full barrier.
-template <int D>
-__device__ __forceinline__ void issue_qk(uint8_t* smem, uint32_t tmem, int u, int j, uint64_t* s_full_u) {
-  using L = Layout<D>;
-  constexpr uint32_t kSwizzleQK = (D == 128) ? 4u : 6u;  // 64-B or 32-B rows
-  constexpr uint32_t kSbo = 8 * L::kRowBytes;
-  constexpr uint32_t idesc_qk = idesc_fp4_block_scaled(128, 128, 0, 0, 0);
-  const int s = j % kStages;
-  const uint32_t sfk = tmem + kColSFK + 16 * u + 8 * (j & 1);
-  const uint32_t sfq = tmem + kColSFQ + 8 * u;
-  const uint64_t qdesc = smem_desc(smem_u32(smem + L::kQ + u * L::kTileQK), 16, kSbo, kSwizzleQK);
-  const uint64_t kdesc = smem_desc(smem_u32(smem + L::kK + s * L::kTileQK), 16, kSbo, kSwizzleQK);
-#pragma unroll
-  for (int a = 0; a < L::kSFAtoms; ++a) tc_cp_sf_atom(sfk + 4 * a, smem + L::kSFK + (s * L::kSFAtoms + a) * 512);
-#pragma unroll
-  for (int ks = 0; ks < D / 64; ++ks)
-    mma_nvf4(tmem + kColS, qdesc + 2 * ks, kdesc + 2 * ks, idesc_qk, sfq + 4 * ks, sfk + 4 * ks, ks > 0);
-  tc_commit(s_full_u);
-}
-
 template <int D, bool DUMP>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_directp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -151,11 +126,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_kv_full = bars + 1;
   uint64_t* bar_kv_empty = bars + 1 + kStages;
   uint64_t* bar_s_full = bars + 1 + 2 * kStages;  // [2]
-  uint64_t* bar_p_full = bar_s_full + 2;          // [2]
-  uint64_t* bar_o_full = bar_s_full + 4;          // [2]
+  uint64_t* bar_s_free = bar_s_full + 2;          // [2]
+  uint64_t* bar_p_full = bar_s_full + 4;          // [2]
+  uint64_t* bar_o_full = bar_s_full + 6;          // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
-  uint32_t* s_loaded = reinterpret_cast<uint32_t*>(smem + L::kMisc + 8);  // [2] warps that hold their S rows
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qt0 = 2 * blockIdx.x;  // first of the two query tiles
@@ -172,8 +147,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar_s_full + t, 1);
-      mbar_init(bar_p_full + t, 4);  // one arrival per softmax warp
-      s_loaded[t] = 0;
+      mbar_init(bar_s_free + t, 4);  // one arrival per softmax warp
+      mbar_init(bar_p_full + t, 4);
       mbar_init(bar_o_full + t, 1);
     }
     *abort_flag = 0;
@@ -234,14 +209,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(bar_kv_full + (j % kStages), (j / kStages) & 1, abort_flag, p.status, 2);
     mbar_wait(bar_q_full, 0, abort_flag, p.status, 3);
   } else if (warp == kWarpMma0 || (warp == kWarpMma0 + 1 && has1)) {
-    // ------------------------------------------------------------ PV issuers
-    // Warp 9 + t issues the PV products of query tile t.  The whole warp runs
-    // the loop and waits (so descriptors stay warp-uniform); one elected lane
-    // issues each group of tcgen05 operations.  Warp 9 also copies the
-    // constant scale atoms and issues the first S = Q_0 K(0)^T; its commit
-    // covers those copies, so every later user sees them in place.
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 9 + t issues everything of query tile t.  The whole warp runs the
+    // loop and waits (so descriptors stay warp-uniform); one elected lane
+    // issues each group of tcgen05 operations.
     const int t = warp - kWarpMma0;
     const bool leader = elect_one();
+    constexpr uint32_t kSwizzleQK = (D == 128) ? 4u : 6u;  // 64-B or 32-B rows
+    constexpr uint32_t kSbo = 8 * L::kRowBytes;
+    constexpr uint32_t idesc_qk = idesc_fp4_block_scaled(128, 128, 0, 0, 0);
     constexpr uint32_t idesc_pv0 = idesc_fp4_block_scaled(128, D, 1, 0, 0);
     constexpr uint32_t idesc_pv1 = idesc_fp4_block_scaled(128, D, 1, 2, 2);
     constexpr uint32_t idesc_l0 = idesc_fp4_block_scaled(128, kLN, 1, 0, 0);
@@ -249,41 +225,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Descriptors are built once; the start-address field is linear in the
     // shared-memory address (16-byte units), so tiles are reached by adding
     // their offset.
+    const uint64_t qdesc = smem_desc(smem_u32(smem + L::kQ + t * L::kTileQK), 16, kSbo, kSwizzleQK);
+    const uint64_t kdesc0 = smem_desc(smem_u32(smem + L::kK), 16, kSbo, kSwizzleQK);
     const uint64_t vdesc0 = smem_desc(smem_u32(smem + L::kV), 16, 512, 4);
     const uint64_t pdesc = smem_desc(smem_u32(smem + L::kP + t * 8192), 16, 512, 4);
     const uint64_t ones_desc = smem_desc(smem_u32(smem + L::kOnes), 16, 512, 4);
-    constexpr uint64_t kVStep = L::kTileV >> 4;
+    constexpr uint64_t kQKStep = L::kTileQK >> 4, kVStep = L::kTileV >> 4;
+    const uint32_t t_s = tmem + kColS;
     const uint32_t t_o = tmem + kColO + t * D;
     const uint32_t t_l = tmem + kColL + 16 * t;
+    const uint32_t t_sfq = tmem + kColSFQ + 8 * t;
+    const uint32_t t_sfk = tmem + kColSFK + 16 * t;
     const uint32_t t_sfv = tmem + kColSFV + 8 * t;
     const uint32_t t_sfp = tmem + kColSFP + 4 * t;
     const uint32_t t_sf1 = tmem + kColSFOnes + 4 * t;
+    uint64_t* s_full = bar_s_full + t;
     uint64_t* p_full = bar_p_full + t;
     uint64_t* o_full = bar_o_full + t;
     auto wait = [&](uint64_t* bar, uint32_t parity, unsigned site) {
       return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort_flag, p.status, site));
     };
-
-    bool ok = true;
-    if (t == 0) {
-      ok = wait(bar_q_full, 0, 10) && wait(bar_kv_full, 0, 11);
-      if (ok) {
-        tc_fence_after();
-        if (leader) {
-          for (int u = 0; u < (has1 ? 2 : 1); ++u) {
-            for (int a = 0; a < L::kSFAtoms; ++a)
-              tc_cp_sf_atom(tmem + kColSFQ + 8 * u + 4 * a, smem + L::kSFQ + (u * L::kSFAtoms + a) * 512);
-            tc_cp_sf_atom(tmem + kColSFOnes + 4 * u, smem + L::kSFOnes);
-          }
-          issue_qk<D>(smem, tmem, 0, 0, bar_s_full);
-        }
-        __syncwarp();
-      }
-    }
-    for (int j = 0; ok && j < nkv; ++j) {
+    // The score bank is free for S_t(j) once the other tile has pulled its
+    // previous S into registers (tile 0, step j: tile 1's step j-1; tile 1,
+    // step j: tile 0's step j); without a second tile, once tile 0 has pulled
+    // its own previous S.
+    auto bank_free = [&](int j) {  // before S_t(j); j >= 1 for tile 0
+      if (t == 1) return wait(bar_s_free, j & 1, 12);
+      return wait(bar_s_free + (has1 ? 1 : 0), (j - 1) & 1, 13);
+    };
+    auto copy_sfk = [&](int j) {  // K scale atoms of step j into this tile's columns for its parity
       const int s = j % kStages;
-      if (!(ok = wait(p_full, j & 1, 15))) break;
-      tc_fence_after();
+      const uint32_t sfk = t_sfk + 8 * (j & 1);
+      if (leader) {
+#pragma unroll
+        for (int a = 0; a < L::kSFAtoms; ++a)
+          tc_cp_sf_atom(sfk + 4 * a, smem + L::kSFK + (s * L::kSFAtoms + a) * 512);
+      }
+      __syncwarp();
+    };
+    auto issue_qk = [&](int j) {  // S = Q_t K(j)^T (K scale atoms already copied)
+      const int s = j % kStages;
+      const uint32_t sfk = t_sfk + 8 * (j & 1);
+      if (leader) {
+#pragma unroll
+        for (int ks = 0; ks < D / 64; ++ks)
+          mma_nvf4(t_s, qdesc + 2 * ks, kdesc0 + s * kQKStep + 2 * ks, idesc_qk, t_sfq + 4 * ks, sfk + 4 * ks,
+                   ks > 0);
+        tc_commit(s_full);
+      }
+      __syncwarp();
+    };
+    auto issue_pv = [&](int j) {  // P and V scale atoms, O_t += P_t V(j), l_t = P_t 1
+      const int s = j % kStages;
       const uint32_t sfv = t_sfv + 4 * (j & 1);
       const uint64_t vd = vdesc0 + s * kVStep;
       if (leader) {
@@ -297,6 +290,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(bar_kv_empty + s);
       }
       __syncwarp();
+    };
+
+    bool ok = wait(bar_q_full, 0, 10);
+    if (ok) {
+      tc_fence_after();
+      if (leader) {
+        for (int a = 0; a < L::kSFAtoms; ++a)
+          tc_cp_sf_atom(t_sfq + 4 * a, smem + L::kSFQ + (t * L::kSFAtoms + a) * 512);
+        tc_cp_sf_atom(t_sf1, smem + L::kSFOnes);
+      }
+      __syncwarp();
+      ok = wait(bar_kv_full, 0, 11);
+    }
+    if (ok) {
+      tc_fence_after();
+      copy_sfk(0);
+    }
+    if (ok && t == 1) ok = wait(bar_s_free, 0, 12);  // tile 0 has pulled S_0(0)
+    if (ok) {
+      tc_fence_after();
+      issue_qk(0);
+    }
+    // Per KV step j: the next scores first (they need only K(j+1) and the
+    // bank; the K scale atoms go in before the bank is waited for), then this
+    // tile's PV product of step j.
+    for (int j = 0; ok && j < nkv; ++j) {
+      if (j + 1 < nkv) {
+        if (!(ok = wait(bar_kv_full + (j + 1) % kStages, ((j + 1) / kStages) & 1, 14))) break;
+        tc_fence_after();
+        copy_sfk(j + 1);
+        if (!(ok = bank_free(j + 1))) break;
+        tc_fence_after();
+        issue_qk(j + 1);
+      }
+      if (!(ok = wait(p_full, j & 1, 15))) break;
+      tc_fence_after();
+      issue_pv(j);
     }
   } else if (warp < 8 && (warp < 4 || has1)) {
     // ------------------------------------------------------------ softmax rows
@@ -308,6 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + lane_base + kColO + t * D;
     const uint32_t tL = tmem + lane_base + kColL + 16 * t;
     uint64_t* s_full = bar_s_full + t;
+    uint64_t* s_free = bar_s_free + t;
     uint64_t* p_full = bar_p_full + t;
     uint64_t* o_full = bar_o_full + t;
     uint8_t* sP = smem + L::kP + t * 8192;
@@ -336,22 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bm[2] = tmem_ld32_max(tS + 64, *reinterpret_cast<float(*)[32]>(s + 64));
       bm[3] = tmem_ld32_max(tS + 96, *reinterpret_cast<float(*)[32]>(s + 96));
       tmem_wait_ld();
-      // Once all four warps hold their rows, the bank is free.  Each warp
-      // counts itself in; the last of the four issues the next S into the
-      // bank -- for the other tile at the same step (tile 0 -> tile 1) or the
-      // next step (tile 1 -> tile 0), or for this tile's next step when there
-      // is no second tile.  Nobody waits for anybody here.
       tc_fence_before();
       __syncwarp();
-      if (lane == 0 && (smem_atomic_add_acq_rel(s_loaded + t, 1u) & 3u) == 3u) {
-        const int u = has1 ? 1 - t : 0;
-        const int jn = (has1 && t == 0) ? j : j + 1;
-        if (jn < nkv && mbar_wait(bar_kv_full + jn % kStages, (jn / kStages) & 1, abort_flag, p.status, 23)) {
-          tc_fence_after();
-          issue_qk<D>(smem, tmem, u, jn, bar_s_full + u);
-        }
-      }
-      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free);
 
       const int valid = N - j * 128;  // keys of this tile that exist (>= 1)
       if (valid < 128) {
