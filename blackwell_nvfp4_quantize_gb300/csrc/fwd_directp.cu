@@ -21,12 +21,13 @@
 //              each; warp 9 also owns the TMEM allocation):
 //              S   = Q_t K^T     kind::mxf4nvf4, 16-element UE4M3 scales
 //              O_t += P_t V      kind::mxf4, 32-element UE8M0 scales
-//   The denominator is summed by the softmax threads from the same codes and
-//   block scales they hand to the PV product (a byte-permute decode of the
-//   packed codes, exact block sums, one fp32 accumulation per block).
+//              l_t  = P_t 1      the same P operand against a tile of E2M1
+//                                ones: the tile's denominator from exactly the
+//                                codes and scales the PV product consumes; the
+//                                softmax warps add it up in fp32 registers
 // TMEM (512 columns): one score bank S shared by the two tiles (a softmax
 // warpgroup copies S to registers and releases the bank at once), two output
-// banks, and the scale-factor columns.
+// banks, two 16-column l banks, and the scale-factor columns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -48,11 +49,14 @@ static_assert(kStages >= 2, "the K/V ring needs at least two stages");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;         // 128 columns: fp32 scores of 128 keys
 constexpr uint32_t kColO = 128;       // tile t output at kColO + t * D
-constexpr uint32_t kColSFQ = 384;     // tile t Q scale atoms at kColSFQ + 8 t
-constexpr uint32_t kColSFK = 400;     // tile t, KV-step parity q: kColSFK + 16 t + 8 q
-constexpr uint32_t kColSFV = 432;     // tile t, KV-step parity q: kColSFV + 8 t + 4 q
-constexpr uint32_t kColSFP = 448;     // tile t P scale atom at kColSFP + 4 t
-static_assert(kColSFP + 8 <= kTmemCols, "TMEM plan exceeds 512 columns");
+constexpr uint32_t kColL = 384;       // tile t denominator at kColL + 16 t
+constexpr uint32_t kColSFQ = 416;     // tile t Q scale atoms at kColSFQ + 8 t
+constexpr uint32_t kColSFK = 432;     // tile t, KV-step parity q: kColSFK + 16 t + 8 q
+constexpr uint32_t kColSFV = 464;     // tile t, KV-step parity q: kColSFV + 8 t + 4 q
+constexpr uint32_t kColSFP = 480;     // tile t P scale atom at kColSFP + 4 t
+constexpr uint32_t kColSFOnes = 488;  // tile t unit scales of the ones tile at kColSFOnes + 4 t
+static_assert(kColSFOnes + 8 <= kTmemCols, "TMEM plan exceeds 512 columns");
+constexpr uint32_t kLN = 16;                     // N of the denominator MMA
 constexpr float kLog2Six = 2.5849625007211561f;  // log2(6) rounded to fp32
 constexpr double kLog2E = 1.4426950408889634074;
 // The reference maximum M of a row moves (and O, l are rescaled by an exact
@@ -70,11 +74,13 @@ struct Layout {
   static constexpr int kK = kQ + 2 * kTileQK;
   static constexpr int kV = kK + kStages * kTileQK;
   static constexpr int kP = kV + kStages * kTileV;  // two P tiles of 128 x 64 bytes
-  static constexpr int kSFQ = kP + 2 * 8192;
+  static constexpr int kOnes = kP + 2 * 8192;       // 16 rows x 64 bytes of E2M1 ones
+  static constexpr int kSFQ = kOnes + 1024;
   static constexpr int kSFK = kSFQ + 2 * kSFAtoms * 512;
   static constexpr int kSFV = kSFK + kStages * kSFAtoms * 512;
   static constexpr int kSFP = kSFV + kStages * 512;
-  static constexpr int kBars = kSFP + 2 * 512;
+  static constexpr int kSFOnes = kSFP + 2 * 512;
+  static constexpr int kBars = kSFOnes + 512;
   static constexpr int kNumBars = 1 + 2 * kStages + 8;  // q, kv full/empty, s_full/s_free/p_full/o_full x2
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
@@ -106,14 +112,6 @@ __device__ __forceinline__ float exp2_int(int e) {  // 2^e, e >= -149
   if (e >= -126) return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
   if (e >= -149) return __uint_as_float(1u << (e + 149));
   return 0.0f;
-}
-
-// Sum of the decoded values of eight non-negative E2M1 codes, in units of 0.5,
-// as four byte lanes (each lane <= 24): a byte-permute table lookup.
-__device__ __forceinline__ uint32_t e2m1x8_halfsum_lanes(uint32_t w) {
-  constexpr uint32_t lo = 0x03020100u;  // 2 x {0, .5, 1, 1.5}
-  constexpr uint32_t hi = 0x0C080604u;  // 2 x {2, 3, 4, 6}
-  return __byte_perm(lo, hi, w & 0xFFFFu) + __byte_perm(lo, hi, w >> 16);
 }
 
 template <int D, bool DUMP>
@@ -156,6 +154,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // constant operands of the denominator MMA: E2M1 ones (0x22 = two 1.0 codes)
+  // and unit E8M0 scales (0x7F = 2^0)
+  for (int i = threadIdx.x; i < 1024 / 16; i += kThreads)
+    reinterpret_cast<uint4*>(smem + L::kOnes)[i] = make_uint4(0x22222222u, 0x22222222u, 0x22222222u, 0x22222222u);
+  for (int i = threadIdx.x; i < 512 / 16; i += kThreads)
+    reinterpret_cast<uint4*>(smem + L::kSFOnes)[i] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+  fence_proxy_async_smem();
   if (warp == kWarpMma0) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
@@ -215,6 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc_qk = idesc_fp4_block_scaled(128, 128, 0, 0, 0);
     constexpr uint32_t idesc_pv0 = idesc_fp4_block_scaled(128, D, 1, 0, 0);
     constexpr uint32_t idesc_pv1 = idesc_fp4_block_scaled(128, D, 1, 2, 2);
+    constexpr uint32_t idesc_l0 = idesc_fp4_block_scaled(128, kLN, 1, 0, 0);
+    constexpr uint32_t idesc_l1 = idesc_fp4_block_scaled(128, kLN, 1, 2, 2);
     // Descriptors are built once; the start-address field is linear in the
     // shared-memory address (16-byte units), so tiles are reached by adding
     // their offset.
@@ -222,13 +229,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t kdesc0 = smem_desc(smem_u32(smem + L::kK), 16, kSbo, kSwizzleQK);
     const uint64_t vdesc0 = smem_desc(smem_u32(smem + L::kV), 16, 512, 4);
     const uint64_t pdesc = smem_desc(smem_u32(smem + L::kP + t * 8192), 16, 512, 4);
+    const uint64_t ones_desc = smem_desc(smem_u32(smem + L::kOnes), 16, 512, 4);
     constexpr uint64_t kQKStep = L::kTileQK >> 4, kVStep = L::kTileV >> 4;
     const uint32_t t_s = tmem + kColS;
     const uint32_t t_o = tmem + kColO + t * D;
+    const uint32_t t_l = tmem + kColL + 16 * t;
     const uint32_t t_sfq = tmem + kColSFQ + 8 * t;
     const uint32_t t_sfk = tmem + kColSFK + 16 * t;
     const uint32_t t_sfv = tmem + kColSFV + 8 * t;
     const uint32_t t_sfp = tmem + kColSFP + 4 * t;
+    const uint32_t t_sf1 = tmem + kColSFOnes + 4 * t;
     uint64_t* s_full = bar_s_full + t;
     uint64_t* p_full = bar_p_full + t;
     uint64_t* o_full = bar_o_full + t;
@@ -265,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     };
-    auto issue_pv = [&](int j) {  // P and V scale atoms, then O_t += P_t V(j)
+    auto issue_pv = [&](int j) {  // P and V scale atoms, O_t += P_t V(j), l_t = P_t 1
       const int s = j % kStages;
       const uint32_t sfv = t_sfv + 4 * (j & 1);
       const uint64_t vd = vdesc0 + s * kVStep;
@@ -274,6 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_cp_sf_atom(sfv, smem + L::kSFV + s * 512);
         mma_mxf4(t_o, pdesc, vd, idesc_pv0, t_sfp, sfv, j > 0);
         mma_mxf4(t_o, pdesc + 2, vd + 2, idesc_pv1, t_sfp, sfv, true);
+        mma_mxf4(t_l, pdesc, ones_desc, idesc_l0, t_sfp, t_sf1, false);
+        mma_mxf4(t_l, pdesc + 2, ones_desc + 2, idesc_l1, t_sfp, t_sf1, true);
         tc_commit(o_full);
         tc_commit(bar_kv_empty + s);
       }
@@ -286,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (leader) {
         for (int a = 0; a < L::kSFAtoms; ++a)
           tc_cp_sf_atom(t_sfq + 4 * a, smem + L::kSFQ + (t * L::kSFAtoms + a) * 512);
+        tc_cp_sf_atom(t_sf1, smem + L::kSFOnes);
       }
       __syncwarp();
       ok = wait(bar_kv_full, 0, 11);
@@ -323,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + kColS;
     const uint32_t tO = tmem + lane_base + kColO + t * D;
+    const uint32_t tL = tmem + lane_base + kColL + 16 * t;
     uint64_t* s_full = bar_s_full + t;
     uint64_t* s_free = bar_s_free + t;
     uint64_t* p_full = bar_p_full + t;
@@ -393,7 +407,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Direct-P: codes of 2^(X - K_b) = 2^(c*s - K_b), eight per word
       uint32_t w[16];
       uint32_t sfword = 0;
-      float l_tile = 0.0f;  // relative to 2^m_ref
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
         const float nk = static_cast<float>(-kb[b]);
@@ -411,14 +424,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         e = e < -127 ? -127 : e;
         const uint32_t byte = (xb[b] == -INFINITY) ? 0u : static_cast<uint32_t>(e + 127);
         sfword |= byte << (8 * b);
-        // denominator: this block's decoded codes (an exact integer count of
-        // halves, <= 384) at the block's scale 2^e
-        const uint32_t lanes = e2m1x8_halfsum_lanes(w[4 * b]) + e2m1x8_halfsum_lanes(w[4 * b + 1]) +
-                               e2m1x8_halfsum_lanes(w[4 * b + 2]) + e2m1x8_halfsum_lanes(w[4 * b + 3]);
-        l_tile += static_cast<float>(__dp4a(static_cast<int>(lanes), 0x01010101, 0)) * exp2_int(e - 1);
       }
       // The previous PV product must be done before this tile's P buffer and
-      // the O bank are touched; it normally finished long ago.
+      // the O / l banks are touched; it normally finished long ago.  Its tile
+      // denominator (relative to the reference it was made with) joins l.
+      float l_prev = 0.0f;
       if (j > 0) {
         ok = mbar_wait(o_full, (j - 1) & 1, abort_flag, p.status, 21);
         if (!__all_sync(0xFFFFFFFFu, ok)) {
@@ -426,12 +436,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
+        l_prev = tmem_ld1(tL);  // completes at a wait below
       }
-      // Rescale O and l of the rows whose reference maximum moved; the whole
-      // warp takes part in the TMEM round trip, other rows multiply by 1.
-      const float f = rescale ? exp2_int(m_old - m_ref) : 1.0f;
-      l_run = l_run * f + l_tile;
+      // Rescale O of the rows whose reference maximum moved; the whole warp
+      // takes part in the TMEM round trip, other rows multiply by 1.
       if (__any_sync(0xFFFFFFFFu, rescale)) {
+        tmem_wait_ld();
+        l_run += l_prev;
+        l_prev = 0.0f;
+        const float f = rescale ? exp2_int(m_old - m_ref) : 1.0f;
+        l_run *= f;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           float o[32];
@@ -458,6 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int b = 0; b < 4; ++b) p.dump_kshift[rr * (p.ntiles * 4) + j * 4 + b] = kb[b];
       }
+      tmem_wait_ld();
+      l_run += l_prev;
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -467,7 +483,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = mbar_wait(o_full, (nkv - 1) & 1, abort_flag, p.status, 22);
     if (__all_sync(0xFFFFFFFFu, ok)) {
       tc_fence_after();
-      const float l = l_run;
+      const float l = l_run + tmem_ld1(tL);
+      tmem_wait_ld();
       const float inv_l = 1.0f / l;
       const bool store = qrow < N;
       __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * N + (store ? qrow : 0)) * D;
