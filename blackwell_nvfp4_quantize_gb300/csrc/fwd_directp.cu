@@ -8,7 +8,7 @@
 //
 // One CTA computes two 128-row query tiles of one (b, h) and streams the key /
 // value tiles of that head through a TMA ring; both query tiles consume every
-// K/V tile.  Roles (352 threads):
+// K/V tile.  Roles (384 threads):
 //   warps 0-3, 4-7  softmax warpgroups, one per query tile, one thread per
 //              query row.  Each reads its S row from TMEM (block maxima come
 //              out of tcgen05.ld.red), maps the scores to E2M1 codes (packed
@@ -16,7 +16,9 @@
 //              and E8M0 scale atom to shared memory, rescales its O
 //              accumulator when the reference maximum moves, and finally
 //              writes O and LSE.
-//   warp 8     TMA producer (one elected lane issues).
+//   warp 11    TMA producer (one elected lane issues; it sleeps between
+//              polls, so it takes no issue slots from the softmax warps of
+//              its SM sub-partition).  Warp 8 has no role.
 //   warps 9,10 tcgen05 MMA issuers, one per query tile (one elected lane
 //              each; warp 9 also owns the TMEM allocation):
 //              S   = Q_t K^T     kind::mxf4nvf4, 16-element UE4M3 scales
@@ -40,8 +42,8 @@
 namespace fp4attn {
 namespace {
 
-constexpr int kThreads = 352;
-constexpr int kWarpTma = 8, kWarpMma0 = 9;  // warps 9 and 10 issue the MMAs of query tiles 0 and 1
+constexpr int kThreads = 384;
+constexpr int kWarpMma0 = 9, kWarpTma = 11;  // warps 9 and 10 issue the MMAs of query tiles 0 and 1
 constexpr int kStages = 3;
 // The MMA warp of a tile issues S = Q K(j+1)^T before its PV product of tile
 // j, so the ring must hold tiles j and j+1 at once.
@@ -189,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < nkv; ++j) {
       const int s = j % kStages;
       if (j >= kStages) {
-        const bool ok = mbar_wait(bar_kv_empty + s, ((j / kStages) - 1) & 1, abort_flag, p.status, 1);
+        const bool ok = mbar_wait_backoff(bar_kv_empty + s, ((j / kStages) - 1) & 1, abort_flag, p.status, 1, 256);
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
       }
       if (leader) {

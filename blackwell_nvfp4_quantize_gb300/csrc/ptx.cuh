@@ -85,6 +85,27 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
+// Bounded wait for a role that is never on the critical path (the TMA
+// producer runs stages ahead): between polls it sleeps, leaving the issue
+// slots of its SM sub-partition to the warps that are.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                  DeviceStatus* status, unsigned site, uint32_t sleep_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    __nanosleep(sleep_ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > FP4ATTN_WAIT_NS) {
+      *abort = 1;
+      if (status) {
+        if (atomicCAS(&status->timeout, 0u, 1u) == 0u) status->where = site;
+      }
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
