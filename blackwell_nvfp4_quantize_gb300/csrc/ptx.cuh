@@ -56,12 +56,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait on a phase parity.  Gives up when *abort becomes nonzero (some
 // other role gave up) or after FP4ATTN_WAIT_NS; in the latter case records the
 // failure and raises *abort.
+// Polls in bursts: the clock and the abort flag are read only every 32 polls,
+// so a phase that completes is seen within a few polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           DeviceStatus* status, unsigned site) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
     if (globaltimer_ns() - t0 > FP4ATTN_WAIT_NS) {
       *abort = 1;
