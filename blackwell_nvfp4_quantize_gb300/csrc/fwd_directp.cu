@@ -8,7 +8,7 @@
 //
 // One CTA computes two 128-row query tiles of one (b, h) and streams the key /
 // value tiles of that head through a TMA ring; both query tiles consume every
-// K/V tile.  Roles (384 threads):
+// K/V tile.  Roles (352 threads):
 //   warps 0-3, 4-7  softmax warpgroups, one per query tile, one thread per
 //              query row.  Each reads its S row from TMEM (block maxima come
 //              out of tcgen05.ld.red), maps the scores to E2M1 codes (packed
@@ -16,9 +16,7 @@
 //              and E8M0 scale atom to shared memory, rescales its O
 //              accumulator when the reference maximum moves, and finally
 //              writes O and LSE.
-//   warp 11    TMA producer (one elected lane issues; it sleeps between
-//              polls, so it takes no issue slots from the softmax warps of
-//              its SM sub-partition).  Warp 8 has no role.
+//   warp 8     TMA producer (one elected lane issues).
 //   warps 9,10 tcgen05 MMA issuers, one per query tile (one elected lane
 //              each; warp 9 also owns the TMEM allocation):
 //              S   = Q_t K^T     kind::mxf4nvf4, 16-element UE4M3 scales
@@ -42,8 +40,8 @@
 namespace fp4attn {
 namespace {
 
-constexpr int kThreads = 384;
-constexpr int kWarpMma0 = 9, kWarpTma = 11;  // warps 9 and 10 issue the MMAs of query tiles 0 and 1
+constexpr int kThreads = 352;
+constexpr int kWarpTma = 8, kWarpMma0 = 9;  // warps 9 and 10 issue the MMAs of query tiles 0 and 1
 constexpr int kStages = 3;
 // The MMA warp of a tile issues S = Q K(j+1)^T before its PV product of tile
 // j, so the ring must hold tiles j and j+1 at once.
@@ -191,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < nkv; ++j) {
       const int s = j % kStages;
       if (j >= kStages) {
-        const bool ok = mbar_wait_backoff(bar_kv_empty + s, ((j / kStages) - 1) & 1, abort_flag, p.status, 1, 256);
+        const bool ok = mbar_wait(bar_kv_empty + s, ((j / kStages) - 1) & 1, abort_flag, p.status, 1);
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
       }
       if (leader) {
@@ -255,20 +253,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t == 1) return wait(bar_s_free, j & 1, 12);
       return wait(bar_s_free + (has1 ? 1 : 0), (j - 1) & 1, 13);
     };
-    auto copy_sfk = [&](int j) {  // K scale atoms of step j into this tile's columns for its parity
+    auto issue_qk = [&](int j) {  // K scale atoms of step j, then S = Q_t K(j)^T
       const int s = j % kStages;
       const uint32_t sfk = t_sfk + 8 * (j & 1);
       if (leader) {
 #pragma unroll
         for (int a = 0; a < L::kSFAtoms; ++a)
           tc_cp_sf_atom(sfk + 4 * a, smem + L::kSFK + (s * L::kSFAtoms + a) * 512);
-      }
-      __syncwarp();
-    };
-    auto issue_qk = [&](int j) {  // S = Q_t K(j)^T (K scale atoms already copied)
-      const int s = j % kStages;
-      const uint32_t sfk = t_sfk + 8 * (j & 1);
-      if (leader) {
 #pragma unroll
         for (int ks = 0; ks < D / 64; ++ks)
           mma_nvf4(t_s, qdesc + 2 * ks, kdesc0 + s * kQKStep + 2 * ks, idesc_qk, t_sfq + 4 * ks, sfk + 4 * ks,
@@ -305,23 +296,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       ok = wait(bar_kv_full, 0, 11);
     }
-    if (ok) {
-      tc_fence_after();
-      copy_sfk(0);
-    }
     if (ok && t == 1) ok = wait(bar_s_free, 0, 12);  // tile 0 has pulled S_0(0)
     if (ok) {
       tc_fence_after();
       issue_qk(0);
     }
     // Per KV step j: the next scores first (they need only K(j+1) and the
-    // bank; the K scale atoms go in before the bank is waited for), then this
-    // tile's PV product of step j.
+    // bank), then this tile's PV product of step j.
     for (int j = 0; ok && j < nkv; ++j) {
       if (j + 1 < nkv) {
         if (!(ok = wait(bar_kv_full + (j + 1) % kStages, ((j + 1) / kStages) & 1, 14))) break;
-        tc_fence_after();
-        copy_sfk(j + 1);
         if (!(ok = bank_free(j + 1))) break;
         tc_fence_after();
         issue_qk(j + 1);

@@ -56,16 +56,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait on a phase parity.  Gives up when *abort becomes nonzero (some
 // other role gave up) or after FP4ATTN_WAIT_NS; in the latter case records the
 // failure and raises *abort.
-// Polls in bursts: the clock and the abort flag are read only every 32 polls,
-// so a phase that completes is seen within a few polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           DeviceStatus* status, unsigned site) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
     if (globaltimer_ns() - t0 > FP4ATTN_WAIT_NS) {
       *abort = 1;
@@ -87,27 +83,6 @@ __device__ __forceinline__ bool elect_one() {
       "selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(pred));
   return pred != 0;
-}
-
-// Bounded wait for a role that is never on the critical path (the TMA
-// producer runs stages ahead): between polls it sleeps, leaving the issue
-// slots of its SM sub-partition to the warps that are.
-__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                                  DeviceStatus* status, unsigned site, uint32_t sleep_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    __nanosleep(sleep_ns);
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (globaltimer_ns() - t0 > FP4ATTN_WAIT_NS) {
-      *abort = 1;
-      if (status) {
-        if (atomicCAS(&status->timeout, 0u, 1u) == 0u) status->where = site;
-      }
-      return false;
-    }
-  }
 }
 
 // ---------------------------------------------------------------- fences
