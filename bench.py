@@ -39,7 +39,9 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic of one forward launch, from an ncu capture (see profiles/), and
 # the hash of the kernel sources it was taken on; reported only while the
 # sources are unchanged.
-TRAFFIC_RECORD = {"sources_sha": None, "bytes_per_launch": None, "note": None}
+TRAFFIC_RECORD = {"sources_sha": "7722b03be3aa9174", "bytes_per_launch": 278279936 + 291816448,
+                  "note": "dram__bytes_read.sum + dram__bytes_write.sum of one launch on the 40-head "
+                          "N=32768 D=128 workload (profiles/fwd_directp_B1_H40_N32768_D128_traffic.md)"}
 KERNEL_SOURCES = ["blackwell_nvfp4_quantize_gb300/csrc/fwd_directp.cu", "blackwell_nvfp4_quantize_gb300/csrc/ptx.cuh"]
 
 
