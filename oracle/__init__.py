@@ -69,12 +69,12 @@ def _load():
     lib.orc_quant_mxfp4_v.argtypes = [u16p, c_int, c_int, c_int, c_int, u8p, u8p, c_int]
     lib.orc_quant_mxfp4_v.restype = None
     lib.orc_directp_rows.argtypes = [u8p, u8p, ctypes.c_float, u8p, u8p, ctypes.c_float, u8p, u8p,
-                                     c_int, c_int, c_int, c_int, ctypes.c_float, i64p, c_int,
+                                     c_int, c_int, c_int, c_int, ctypes.c_float, c_int, i64p, c_int,
                                      f64p, f64p, u8p, i32p, i32p, c_int]
     lib.orc_directp_rows.restype = None
     lib.orc_directp_map_row.argtypes = [f32p, c_int, ctypes.c_float, u8p, i32p, i32p, f64p]
     lib.orc_directp_map_row.restype = None
-    lib.orc_exact_rows.argtypes = [u16p, u16p, u16p, c_int, c_int, c_int, c_int, ctypes.c_double,
+    lib.orc_exact_rows.argtypes = [u16p, u16p, u16p, c_int, c_int, c_int, c_int, ctypes.c_double, c_int,
                                    i64p, c_int, f64p, f64p, c_int]
     lib.orc_exact_rows.restype = None
     _lib = lib
@@ -154,11 +154,11 @@ def quant_mxfp4_v(v_bf16_bits: np.ndarray, threads: int | None = None):
 
 # ---- attention -----------------------------------------------------------
 
-def directp_rows(q, k, v, shape, softmax_scale, rows, threads=None, want_codes=False):
+def directp_rows(q, k, v, shape, softmax_scale, rows, threads=None, want_codes=False, causal=False):
     """Direct-P forward for selected rows.
 
     q, k: (payload, sf, g) as returned by quant_nvfp4; v: (payload_t, sf).
-    rows: int64 flat row ids (b*H + h)*N + i.
+    rows: int64 flat row ids (b*H + h)*N + i.  causal: row i sees keys 0..i.
     Returns dict with o [R,D] f64, lse [R] f64 and, when want_codes, codes
     [R,Npad] u8 (one code per byte), kshift [R,Npad/32] i32, m [R] i32.
     """
@@ -185,7 +185,7 @@ def directp_rows(q, k, v, shape, softmax_scale, rows, threads=None, want_codes=F
         _ptr(qp, ctypes.c_uint8), _ptr(qsf, ctypes.c_uint8), float(gq),
         _ptr(kp, ctypes.c_uint8), _ptr(ksf, ctypes.c_uint8), float(gk),
         _ptr(vp, ctypes.c_uint8), _ptr(vsf, ctypes.c_uint8),
-        B, H, N, D, float(softmax_scale), _ptr(rows, ctypes.c_int64), R,
+        B, H, N, D, float(softmax_scale), int(bool(causal)), _ptr(rows, ctypes.c_int64), R,
         _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
         _ptr(codes, ctypes.c_uint8) if want_codes else null_u8,
         _ptr(kshift, ctypes.c_int32) if want_codes else null_i32,
@@ -208,8 +208,9 @@ def directp_map_row(s: np.ndarray, c: float):
     return codes, ks, int(m.value), float(l.value)
 
 
-def exact_rows(q_bits, k_bits, v_bits, softmax_scale, rows, threads=None):
-    """Unquantized fp64 softmax attention for selected rows of bf16 inputs."""
+def exact_rows(q_bits, k_bits, v_bits, softmax_scale, rows, threads=None, causal=False):
+    """Unquantized fp64 softmax attention for selected rows of bf16 inputs
+    (causal: row i sees keys 0..i)."""
     lib = _load()
     q = np.ascontiguousarray(q_bits, dtype=np.uint16)
     k = np.ascontiguousarray(k_bits, dtype=np.uint16)
@@ -220,7 +221,7 @@ def exact_rows(q_bits, k_bits, v_bits, softmax_scale, rows, threads=None):
     o = np.zeros((R, D), dtype=np.float64)
     lse = np.zeros((R,), dtype=np.float64)
     lib.orc_exact_rows(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16), _ptr(v, ctypes.c_uint16),
-                       B, H, N, D, float(softmax_scale), _ptr(rows, ctypes.c_int64), R,
+                       B, H, N, D, float(softmax_scale), int(bool(causal)), _ptr(rows, ctypes.c_int64), R,
                        _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
                        threads or default_threads())
     return o, lse

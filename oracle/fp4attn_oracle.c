@@ -334,6 +334,7 @@ typedef struct {
     const uint8_t *qp, *qsf, *kp, *ksf, *vp, *vsf;
     float gq, gk, c;
     int B, H, N, D;
+    int causal; /* row i sees keys 0..i only */
     /* per-head decoded operands */
     long bh;
     double *khat; /* [N][D] */
@@ -389,7 +390,9 @@ static void attn_rows_chunk(void *p, long lo, long hi) {
             uint8_t sfb = a->qsf[orc_sf_index((size_t)a->bh, row_tiles(N), i, d / 16, KB)];
             qhat[d] = orc_e2m1_decode(code) * orc_e4m3_decode(sfb);
         }
-        for (int j = 0; j < N; j++) {
+        /* the keys this row sees: all of them, or (causal) keys 0..i */
+        const int nk = a->causal ? i + 1 : N;
+        for (int j = 0; j < nk; j++) {
             double s = 0.0;
             for (int d = 0; d < D; d++) s += qhat[d] * a->khat[(size_t)j * D + d];
             s32[j] = (float)s;
@@ -398,9 +401,9 @@ static void attn_rows_chunk(void *p, long lo, long hi) {
         memset(ks, 0, sizeof(int32_t) * (size_t)(Npad / 32));
         int32_t M;
         double l;
-        orc_directp_map_row(s32, N, a->c, codes, ks, &M, &l);
+        orc_directp_map_row(s32, nk, a->c, codes, ks, &M, &l);
         for (int d = 0; d < D; d++) acc[d] = 0.0;
-        for (int j = 0; j < N; j++) {
+        for (int j = 0; j < nk; j++) {
             int e = ks[j / 32] - M;
             if (e < -127) e = -127;
             double pj = orc_e2m1_decode(codes[j]) * ldexp(1.0, e);
@@ -423,7 +426,7 @@ static void attn_rows_chunk(void *p, long lo, long hi) {
 void orc_directp_rows(const uint8_t *q_payload, const uint8_t *q_sf, float g_q,
                       const uint8_t *k_payload, const uint8_t *k_sf, float g_k,
                       const uint8_t *v_payload_t, const uint8_t *v_sf,
-                      int B, int H, int N, int D, float softmax_scale,
+                      int B, int H, int N, int D, float softmax_scale, int causal,
                       const int64_t *rows, int nrows,
                       double *o, double *lse,
                       uint8_t *codes, int32_t *kshift, int32_t *mrow,
@@ -442,6 +445,7 @@ void orc_directp_rows(const uint8_t *q_payload, const uint8_t *q_sf, float g_q,
     a.H = H;
     a.N = N;
     a.D = D;
+    a.causal = causal;
     /* the log2-domain score multiplier, rounded once to fp32 */
     a.c = (float)((((double)softmax_scale * LOG2E) * (double)g_q) * (double)g_k);
     a.rows = rows;
@@ -482,6 +486,7 @@ typedef struct {
     const uint16_t *q, *k, *v;
     int N, D;
     double scale;
+    int causal;
     const int64_t *rows;
     double *o, *lse;
 } exact_ctx;
@@ -494,8 +499,9 @@ static void exact_chunk(void *p, long lo, long hi) {
         long flat = (long)a->rows[r];
         long bh = flat / N;
         const uint16_t *qr = a->q + (size_t)flat * D;
+        const int nk = a->causal ? (int)(flat % N) + 1 : N; /* keys the row sees */
         double M = -INFINITY;
-        for (int j = 0; j < N; j++) {
+        for (int j = 0; j < nk; j++) {
             const uint16_t *kr = a->k + ((size_t)bh * N + (size_t)j) * D;
             double s = 0.0;
             for (int d = 0; d < D; d++) s += (double)bf16_to_float(qr[d]) * (double)bf16_to_float(kr[d]);
@@ -503,13 +509,13 @@ static void exact_chunk(void *p, long lo, long hi) {
             if (x[j] > M) M = x[j];
         }
         double l = 0.0;
-        for (int j = 0; j < N; j++) {
+        for (int j = 0; j < nk; j++) {
             x[j] = exp2(x[j] - M);
             l += x[j];
         }
         for (int d = 0; d < D; d++) {
             double acc = 0.0;
-            for (int j = 0; j < N; j++)
+            for (int j = 0; j < nk; j++)
                 acc += x[j] * (double)bf16_to_float(a->v[((size_t)bh * N + (size_t)j) * D + d]);
             a->o[(size_t)r * D + d] = acc / l;
         }
@@ -519,11 +525,11 @@ static void exact_chunk(void *p, long lo, long hi) {
 }
 
 void orc_exact_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                    int B, int H, int N, int D, double softmax_scale,
+                    int B, int H, int N, int D, double softmax_scale, int causal,
                     const int64_t *rows, int nrows, double *o, double *lse,
                     int nthreads) {
     (void)B;
     (void)H;
-    exact_ctx a = {q, k, v, N, D, softmax_scale, rows, o, lse};
+    exact_ctx a = {q, k, v, N, D, softmax_scale, causal, rows, o, lse};
     parallel_for(nrows, nthreads, exact_chunk, &a);
 }

@@ -88,8 +88,10 @@ size_t orc_mxfp4_sf_bytes(int B, int H, int N, int D);
 void orc_quant_mxfp4_v(const uint16_t *v, int B, int H, int N, int D,
                        uint8_t *payload_t, uint8_t *sf, int nthreads);
 
-/* ---- Direct-P attention (noncausal), two-pass restatement ----
- * For each requested row i of head bh (rows[r] = bh*N + i):
+/* ---- Direct-P attention, two-pass restatement ----
+ * For each requested row i of head bh (rows[r] = bh*N + i), over the keys j
+ * the row sees -- all N, or with causal != 0 ("What the paper found": the
+ * causal training forward) keys 0..i only:
  *   S_ij   = sum_d qhat_id * khat_jd                    (fp64, exact here)
  *   c      = fp32( softmax_scale * log2(e) * g_Q * g_K ) (fp64 products)
  *   X_ij   = fp32( c * fp32(S_ij) )
@@ -101,13 +103,16 @@ void orc_quant_mxfp4_v(const uint16_t *v, int B, int H, int N, int D,
  *   l_i    = sum_j p_ij,  O_i = sum_j p_ij vhat_j / l_i,
  *   LSE_i  = ln2 * (M_i + log2 l_i)
  * Outputs per requested row: O (D doubles), lse, and optionally the codes
- * (Npad bytes, one code per byte, padded keys 0), K_b (Npad/32 int32) and M.
+ * (Npad bytes, one code per byte, padded and unseen keys 0), K_b (Npad/32
+ * int32, 0 for blocks the row does not see) and M.
  * Pinned: rows of p/l sum to 1, all-equal scores, integer-shift invariance,
- * hand-worked rows (golden), and P-hat @ V-hat recomputation. */
+ * hand-worked rows (golden), and P-hat @ V-hat recomputation; causal: the
+ * last row equals the noncausal row, row 0 returns v-hat_0 exactly, and a
+ * row equals the noncausal last row of the sequence cut after it. */
 void orc_directp_rows(const uint8_t *q_payload, const uint8_t *q_sf, float g_q,
                       const uint8_t *k_payload, const uint8_t *k_sf, float g_k,
                       const uint8_t *v_payload_t, const uint8_t *v_sf,
-                      int B, int H, int N, int D, float softmax_scale,
+                      int B, int H, int N, int D, float softmax_scale, int causal,
                       const int64_t *rows, int nrows,
                       double *o, double *lse,
                       uint8_t *codes, int32_t *kshift, int32_t *mrow,
@@ -121,11 +126,12 @@ void orc_directp_map_row(const float *s, int n, float c,
                          uint8_t *codes, int32_t *kshift, int32_t *m_out,
                          double *l_out);
 
-/* Unquantized softmax attention for the same rows, fp64 throughout, on the
- * bf16 inputs: X = softmax_scale*log2(e)*q.k, M = max X, p = 2^(X-M).
- * Pinned: equals a library softmax-attention to 1e-12 (Stage A). */
+/* Unquantized softmax attention for the same rows (causal as above), fp64
+ * throughout, on the bf16 inputs: X = softmax_scale*log2(e)*q.k, M = max X,
+ * p = 2^(X-M).  Pinned: equals a library softmax-attention to 1e-12
+ * (Stage A), with and without the causal mask. */
 void orc_exact_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                    int B, int H, int N, int D, double softmax_scale,
+                    int B, int H, int N, int D, double softmax_scale, int causal,
                     const int64_t *rows, int nrows, double *o, double *lse,
                     int nthreads);
 
