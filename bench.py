@@ -12,9 +12,12 @@ quoted on.  Its inputs (1 GB bf16, 0.6 GB quantized) exceed the 129 MB L2, so
 no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload I] [--causal]
 
 --impl reference times the CPU oracle (the plain C restatement used by the
 tests) on a bounded sample of the same workload; it is a reported baseline.
+--causal times the causal forward instead (query i sees keys 0..i); its
+FLOPs are counted over the unmasked (query, key) pairs, 4*D*N*(N+1)/2 per head.
 """
 from __future__ import annotations
 
@@ -31,6 +34,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "Direct-P FP4 attn fwd TFLOP/s (4BHN²D/t), % of GB300 dense FP4 peak"
+METRIC_CAUSAL = "Causal Direct-P FP4 attn fwd TFLOP/s (4BHD·N(N+1)/2 / t), % of GB300 dense FP4 peak"
 UNIT = "TFLOP/s"
 # Dense FP4 : dense BF16 tensor throughput on GB300, nominal 13.5 : 2.25 PFLOP/s.
 FP4_OVER_BF16 = 13.5 / 2.25
@@ -118,7 +122,16 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(w, q, k, v, budget_s=12.0):
+def attn_flops(rows, N, D, causal):
+    """4*D per (query, key) pair the rows attend to: N keys each, or i+1 for row i (causal)."""
+    import numpy as np
+
+    rows = np.asarray(rows, dtype=np.int64)
+    keys = (rows % N + 1).sum() if causal else rows.size * N
+    return 4.0 * D * float(keys)
+
+
+def cpu_baseline(w, q, k, v, causal=False, budget_s=12.0):
     """The oracle as it stands, on host cores, on a bounded row sample of head 0."""
     import numpy as np
 
@@ -138,16 +151,16 @@ def cpu_baseline(w, q, k, v, budget_s=12.0):
     vq = oracle.quant_mxfp4_v(vb, threads)
     t_quant = time.perf_counter() - t0
     # calibrate, then time a sample sized to the budget
-    probe = np.arange(min(N, 2 * threads), dtype=np.int64)
+    probe = np.linspace(0, N - 1, min(N, 2 * threads)).astype(np.int64)
     t0 = time.perf_counter()
-    oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, probe, threads)
+    oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, probe, threads, causal=causal)
     t_probe = time.perf_counter() - t0
     rows = int(max(len(probe), min(N, len(probe) * budget_s / max(t_probe, 1e-6))))
     sample = np.linspace(0, N - 1, rows).astype(np.int64)
     t0 = time.perf_counter()
-    oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, sample, threads)
+    oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, sample, threads, causal=causal)
     t = time.perf_counter() - t0
-    flops = 4.0 * rows * N * D
+    flops = attn_flops(sample, N, D, causal)
     return {"value": flops / t / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": "%d of %d query rows of head 0 of %s (attention rows only; the oracle's quantization "
                       "of that head took %.1f s and is excluded), %.1f s" % (rows, N, w.name, t_quant, t)}
@@ -169,30 +182,34 @@ def run_reference(args, w):
     qb, kb, vb = (wl.bf16_bits(t[:1, :1].contiguous()) for t in (q, k, v))
     shape1 = (1, 1, N, D)
     qq, kq, vq = oracle.quant_nvfp4(qb, threads), oracle.quant_nvfp4(kb, threads), oracle.quant_mxfp4_v(vb, threads)
+    causal = args.causal
     rows_per_step = max(threads, 2 * threads)
-    probe = np.arange(rows_per_step, dtype=np.int64)
+    probe = np.linspace(0, N - 1, rows_per_step).astype(np.int64)
     t0 = time.perf_counter()
-    oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, probe, threads)
+    oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, probe, threads, causal=causal)
     t_probe = time.perf_counter() - t0
     per_step_budget = max(0.5, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
     rows_per_step = int(max(threads, min(N, rows_per_step * per_step_budget / max(t_probe, 1e-6))))
     rng = np.random.default_rng(0)
     times = []
+    flops = 0.0
     for i in range(args.warmup + args.steps):
         rows = np.sort(rng.choice(N, size=rows_per_step, replace=False)).astype(np.int64)
         t0 = time.perf_counter()
-        oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, rows, threads)
+        oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, rows, threads, causal=causal)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(dt)
+            flops += attn_flops(rows, N, D, causal)
     t = sum(times)
-    flops = 4.0 * rows_per_step * N * D * len(times)
     value = flops / t / 1e12
     sample = "%d query rows per step of head 0 of %s (attention rows; quantization excluded)" % (rows_per_step, w.name)
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+    line = {"metric": METRIC_CAUSAL if causal else METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * t / len(times), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "recipe": w.description},
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "recipe": w.description,
+                       "mask": "causal" if causal else "none"},
             "impl": "reference",
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -225,6 +242,7 @@ def run_ours(args, w):
     o = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     launches_per_step = 3 + 3 + 1 + 1  # amax, quant, finalize (x2), V quant, forward
+    fwd = fa.fwd_directp_causal if args.causal else fa.fwd_directp
 
     fwd_events = []
 
@@ -235,11 +253,11 @@ def run_ours(args, w):
         if record:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            fa.fwd_directp(qq, kq, vq, w.softmax_scale, o=o, lse=lse, stream=stream)
+            fwd(qq, kq, vq, w.softmax_scale, o=o, lse=lse, stream=stream)
             e1.record(stream)
             fwd_events.append((e0, e1))
         else:
-            fa.fwd_directp(qq, kq, vq, w.softmax_scale, o=o, lse=lse, stream=stream)
+            fwd(qq, kq, vq, w.softmax_scale, o=o, lse=lse, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -277,7 +295,7 @@ def run_ours(args, w):
         fa.quant_qk_nvfp4(q, out=qq, stream=stream)
         fa.quant_qk_nvfp4(k, out=kq, stream=stream)
         fa.quant_v_mxfp4(v, out=vq, stream=stream)
-        fa.fwd_directp(qq, kq, vq, w.softmax_scale, o=o, lse=lse, stream=stream)
+        fwd(qq, kq, vq, w.softmax_scale, o=o, lse=lse, stream=stream)
         o_p.copy_(o, non_blocking=True)
         lse_p.copy_(lse, non_blocking=True)
 
@@ -297,7 +315,7 @@ def run_ours(args, w):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_total, e2e_ms = float(t[0]), float(t[1])
 
-    flops = float(w.flops)
+    flops = B * H * attn_flops(range(N), N, D, args.causal)
     ms_step = ms_total / args.steps
     value = world * flops / (ms_step * 1e-3) / 1e12
     fwd_avg = sum(fwd_ms) / len(fwd_ms)
@@ -305,12 +323,16 @@ def run_ours(args, w):
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS)) * FP4_OVER_BF16
     traffic = TRAFFIC_RECORD["bytes_per_launch"] if TRAFFIC_RECORD["sources_sha"] == sources_sha() else None
+    if args.causal:
+        traffic = None  # the recorded capture is of the noncausal forward
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC_CAUSAL if args.causal else METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e2m1", "data": "synthetic",
         "config": {"workload": w.name, "B": B, "H": H, "N": N, "D": D, "recipe": w.description,
-                   "step": "NVFP4 quantize Q and K, MXFP4 quantize V, Direct-P forward",
+                   "step": "NVFP4 quantize Q and K, MXFP4 quantize V, %sDirect-P forward"
+                           % ("causal " if args.causal else ""),
+                   "mask": "causal" if args.causal else "none",
                    "l2": "inputs larger than L2 (1 GB bf16 in, 0.6 GB quantized); no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "fwd_ms": fwd_avg,
@@ -318,16 +340,14 @@ def run_ours(args, w):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": "%s bf16 dense x %.1f (nominal FP4:BF16 dense ratio), burst" % (peak_src, FP4_OVER_BF16),
-                     "kernel": "fwd_directp_kernel<128>"},
+                     "kernel": "fwd_directp_kernel<%d, causal=%s>" % (D, str(bool(args.causal)).lower())},
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": 3 * B * H * N * D * 2, "d2h_bytes_per_step": B * H * N * D * 2 + B * H * N * 4},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, q_h, k_h, v_h)
-    elif rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, q_h, k_h, v_h)
+        line["cpu_baseline"] = cpu_baseline(w, q_h, k_h, v_h, causal=args.causal)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -343,6 +363,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=4, help="workload index 1-5 (default 4)")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--causal", action="store_true", help="time the causal forward (query i sees keys 0..i)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

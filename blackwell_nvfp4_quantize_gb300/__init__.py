@@ -8,7 +8,8 @@ raises if the library has not been built -- there is no fallback.
 Method: "Hardware-Aware FP4 FlashAttention-4" (Direct-P for noncausal
 inference): NVFP4 Q/K, MXFP4 V along keys, scores mapped directly to MXFP4
 E2M1 probability codes, denominator from the same rounded probabilities, O
-and LSE as outputs.
+and LSE as outputs; and its causal training forward, which keeps the
+quantized Q/K and the LSE for a backward pass.
 """
 from __future__ import annotations
 
@@ -69,7 +70,12 @@ def lib():
     L.fp4attn_fwd_directp_noalloc.argtypes = [ctypes.POINTER(_NVFP4), ctypes.POINTER(_NVFP4),
                                               ctypes.POINTER(_MXFP4), vp, vp, i, i, i, i, f, vp]
     L.fp4attn_debug_cvt_transitions.argtypes = [i, ctypes.c_uint32, ctypes.c_uint32, vp, i, vp, vp]
-    for name in ("fp4attn_fwd_directp_noalloc", "fp4attn_debug_cvt_transitions", "fp4attn_nvfp4_bytes", "fp4attn_mxfp4_v_bytes", "fp4attn_quant_qk_nvfp4",
+    L.fp4attn_fwd_directp_causal.argtypes = L.fp4attn_fwd_directp.argtypes
+    L.fp4attn_debug_dump_p_causal.argtypes = L.fp4attn_debug_dump_p.argtypes
+    L.fp4attn_fwd_directp_causal_save.argtypes = [vp, vp, vp, ctypes.POINTER(_NVFP4), ctypes.POINTER(_NVFP4),
+                                                  ctypes.POINTER(_MXFP4), vp, vp, i, i, i, i, f, vp]
+    for name in ("fp4attn_fwd_directp_causal", "fp4attn_debug_dump_p_causal", "fp4attn_fwd_directp_causal_save",
+                 "fp4attn_fwd_directp_noalloc", "fp4attn_debug_cvt_transitions", "fp4attn_nvfp4_bytes", "fp4attn_mxfp4_v_bytes", "fp4attn_quant_qk_nvfp4",
                  "fp4attn_quant_v_mxfp4", "fp4attn_fwd_directp", "fp4attn_debug_dump_p",
                  "fp4attn_device_status"):
         getattr(L, name).restype = i
@@ -174,9 +180,7 @@ def quant_v_mxfp4(v: torch.Tensor, out: MXFP4Tensor | None = None, stream=None) 
     return out
 
 
-def fwd_directp(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP4Tensor, softmax_scale: float | None = None,
-                o: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
-    """fp4attn_fwd_directp: returns (O bf16 [B,H,N,D], LSE fp32 [B,H,N])."""
+def _fwd(name, q, k, v, softmax_scale, o, lse, stream):
     B, H, N, D = q.shape
     dev = q.payload.device
     if softmax_scale is None:
@@ -184,10 +188,46 @@ def fwd_directp(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP4Tensor, softmax_scale: f
     o = o if o is not None else torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev)
     lse = lse if lse is not None else torch.empty((B, H, N), dtype=torch.float32, device=dev)
     qc, kc, vc = q._c(), k._c(), v._c()
-    _check(lib().fp4attn_fwd_directp(ctypes.byref(qc), ctypes.byref(kc), ctypes.byref(vc), _ptr(o), _ptr(lse),
-                                     B, H, N, D, float(softmax_scale), ctypes.c_void_p(_stream(stream))),
-           "fp4attn_fwd_directp")
+    _check(getattr(lib(), name)(ctypes.byref(qc), ctypes.byref(kc), ctypes.byref(vc), _ptr(o), _ptr(lse),
+                                B, H, N, D, float(softmax_scale), ctypes.c_void_p(_stream(stream))), name)
     return o, lse
+
+
+def fwd_directp(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP4Tensor, softmax_scale: float | None = None,
+                o: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
+    """fp4attn_fwd_directp: returns (O bf16 [B,H,N,D], LSE fp32 [B,H,N])."""
+    return _fwd("fp4attn_fwd_directp", q, k, v, softmax_scale, o, lse, stream)
+
+
+def fwd_directp_causal(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP4Tensor, softmax_scale: float | None = None,
+                       o: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
+    """fp4attn_fwd_directp_causal (query i sees keys 0..i): returns (O, LSE)."""
+    return _fwd("fp4attn_fwd_directp_causal", q, k, v, softmax_scale, o, lse, stream)
+
+
+def fwd_directp_causal_save(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scale: float | None = None,
+                            q_saved: NVFP4Tensor | None = None, k_saved: NVFP4Tensor | None = None,
+                            v_quant: MXFP4Tensor | None = None, o: torch.Tensor | None = None,
+                            lse: torch.Tensor | None = None, stream=None):
+    """fp4attn_fwd_directp_causal_save: quantizes Q, K, V and runs the causal
+    forward in one call.  Returns (O, LSE, q_saved, k_saved, v_quant); the
+    quantized Q/K and the LSE are what a backward pass reconstructs P from."""
+    for x, name in ((q, "q"), (k, "k"), (v, "v")):
+        _check_input(x, name)
+    B, H, N, D = q.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    q_saved = q_saved or empty_nvfp4(q.shape, q.device)
+    k_saved = k_saved or empty_nvfp4(k.shape, k.device)
+    v_quant = v_quant or empty_mxfp4(v.shape, v.device)
+    o = o if o is not None else torch.empty((B, H, N, D), dtype=torch.bfloat16, device=q.device)
+    lse = lse if lse is not None else torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    qc, kc, vc = q_saved._c(), k_saved._c(), v_quant._c()
+    _check(lib().fp4attn_fwd_directp_causal_save(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(qc), ctypes.byref(kc),
+                                                 ctypes.byref(vc), _ptr(o), _ptr(lse), B, H, N, D,
+                                                 float(softmax_scale), ctypes.c_void_p(_stream(stream))),
+           "fp4attn_fwd_directp_causal_save")
+    return o, lse, q_saved, k_saved, v_quant
 
 
 def fwd_directp_noalloc(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP4Tensor, o: torch.Tensor, lse: torch.Tensor,
@@ -206,9 +246,9 @@ def fwd_directp_noalloc(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP4Tensor, o: torch
 
 
 def debug_dump_p(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP4Tensor, b: int, h: int, row0: int, nrows: int,
-                 softmax_scale: float | None = None, stream=None):
-    """fp4attn_debug_dump_p: (O, LSE, codes [nrows, Npad/2] u8, kshift [nrows, Npad/32] i32,
-    O of the dumped rows in fp32 [nrows, D])."""
+                 softmax_scale: float | None = None, stream=None, causal: bool = False):
+    """fp4attn_debug_dump_p (or fp4attn_debug_dump_p_causal): (O, LSE, codes [nrows, Npad/2] u8,
+    kshift [nrows, Npad/32] i32, O of the dumped rows in fp32 [nrows, D])."""
     B, H, N, D = q.shape
     dev = q.payload.device
     if softmax_scale is None:
@@ -220,10 +260,10 @@ def debug_dump_p(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP4Tensor, b: int, h: int,
     kshift = torch.zeros((nrows, npad // 32), dtype=torch.int32, device=dev)
     o32 = torch.zeros((nrows, D), dtype=torch.float32, device=dev)
     qc, kc, vc = q._c(), k._c(), v._c()
-    _check(lib().fp4attn_debug_dump_p(ctypes.byref(qc), ctypes.byref(kc), ctypes.byref(vc), _ptr(o), _ptr(lse),
-                                      B, H, N, D, float(softmax_scale), b, h, row0, nrows, _ptr(codes),
-                                      _ptr(kshift), _ptr(o32), ctypes.c_void_p(_stream(stream))),
-           "fp4attn_debug_dump_p")
+    name = "fp4attn_debug_dump_p_causal" if causal else "fp4attn_debug_dump_p"
+    _check(getattr(lib(), name)(ctypes.byref(qc), ctypes.byref(kc), ctypes.byref(vc), _ptr(o), _ptr(lse),
+                                B, H, N, D, float(softmax_scale), b, h, row0, nrows, _ptr(codes),
+                                _ptr(kshift), _ptr(o32), ctypes.c_void_p(_stream(stream))), name)
     return o, lse, codes, kshift, o32
 
 
@@ -245,9 +285,11 @@ def debug_cvt_transitions(fmt: int, lo: int, hi: int, capacity: int = 4096, stre
     return sorted((int(a), int(b)) for a, b in out)
 
 
-def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scale: float | None = None, stream=None):
+def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scale: float | None = None, stream=None,
+              causal: bool = False):
     """Quantize Q, K (NVFP4) and V (MXFP4) and run the Direct-P forward: (O, LSE)."""
     qq = quant_qk_nvfp4(q, stream=stream)
     kq = quant_qk_nvfp4(k, stream=stream)
     vq = quant_v_mxfp4(v, stream=stream)
-    return fwd_directp(qq, kq, vq, softmax_scale, stream=stream)
+    fwd = fwd_directp_causal if causal else fwd_directp
+    return fwd(qq, kq, vq, softmax_scale, stream=stream)

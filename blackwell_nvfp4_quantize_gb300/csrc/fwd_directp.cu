@@ -28,6 +28,13 @@
 // TMEM (512 columns): one score bank S shared by the two tiles (a softmax
 // warpgroup copies S to registers and releases the bank at once), two output
 // banks, two 16-column l banks, and the scale-factor columns.
+//
+// Causal variant (the causal forward of "What the paper found": forward for
+// causal training): key j is seen by query i only when j <= i.  Query tile
+// qt needs the key tiles 0 .. qt, the last one masked along its diagonal, and
+// no others.  CTA c takes the query tiles c and T-1-c (T tiles per head), so
+// every CTA streams T+1 tile-steps of work; the short tile c is tile 0 and
+// drops out after its diagonal, tile T-1-c carries on alone.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -81,7 +88,7 @@ struct Layout {
   static constexpr int kSFP = kSFV + kStages * 512;
   static constexpr int kSFOnes = kSFP + 2 * 512;
   static constexpr int kBars = kSFOnes + 512;
-  static constexpr int kNumBars = 1 + 2 * kStages + 8;  // q, kv full/empty, s_full/s_free/p_full/o_full x2
+  static constexpr int kNumBars = 1 + 2 * kStages + 10;  // q, kv full/empty, s_full/s_free/p_full/o_full/drain x2
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   // Pad the request so that one CTA owns the SM: it allocates all 512 TMEM columns.
@@ -114,7 +121,7 @@ __device__ __forceinline__ float exp2_int(int e) {  // 2^e, e >= -149
   return 0.0f;
 }
 
-template <int D, bool DUMP>
+template <int D, bool DUMP, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_directp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -129,15 +136,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_s_free = bar_s_full + 2;          // [2]
   uint64_t* bar_p_full = bar_s_full + 4;          // [2]
   uint64_t* bar_o_full = bar_s_full + 6;          // [2]
+  uint64_t* bar_drain = bar_s_full + 8;           // [2] the MMA warps' last commit
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt0 = 2 * blockIdx.x;  // first of the two query tiles
   const int bh = blockIdx.y;
   const int N = p.N;
-  const int nkv = p.ntiles;
-  const bool has1 = (qt0 + 1) * 128 < N;  // the second query tile holds rows
+  // Query tiles of this CTA and the number of key tiles each consumes (tile
+  // 1 never consumes fewer than tile 0).
+  const int qt0 = CAUSAL ? static_cast<int>(blockIdx.x) : 2 * static_cast<int>(blockIdx.x);
+  const int qt1 = CAUSAL ? p.ntiles - 1 - qt0 : qt0 + 1;
+  const bool has1 = CAUSAL ? qt1 > qt0 : qt1 * 128 < N;  // the second query tile exists
+  const int nkv0 = CAUSAL ? qt0 + 1 : p.ntiles;
+  const int nkv1 = CAUSAL ? qt1 + 1 : p.ntiles;
+  const int nkv = has1 ? nkv1 : nkv0;  // key tiles streamed through the ring
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q_full, 1);
@@ -150,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_s_free + t, 4);  // one arrival per softmax warp
       mbar_init(bar_p_full + t, 4);
       mbar_init(bar_o_full + t, 1);
+      mbar_init(bar_drain + t, 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -181,11 +195,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_v);
       mbar_arrive_expect_tx(bar_q_full, (has1 ? 2 : 1) * (L::kTileQK + kSfBytes));
       for (int t = 0; t < (has1 ? 2 : 1); ++t) {
-        tma_load_3d(smem + L::kQ + t * L::kTileQK, &tm_q, bar_q_full, 0, (qt0 + t) * 128, bh);
-        bulk_load(smem + L::kSFQ + t * kSfBytes, p.q_sf + (static_cast<size_t>(bh) * p.ntiles + qt0 + t) * kSfBytes,
+        const int qt = t ? qt1 : qt0;
+        tma_load_3d(smem + L::kQ + t * L::kTileQK, &tm_q, bar_q_full, 0, qt * 128, bh);
+        bulk_load(smem + L::kSFQ + t * kSfBytes, p.q_sf + (static_cast<size_t>(bh) * p.ntiles + qt) * kSfBytes,
                   kSfBytes, bar_q_full);
       }
     }
+    int issued = 0;  // key/value tiles whose copies were issued
     for (int j = 0; j < nkv; ++j) {
       const int s = j % kStages;
       if (j >= kStages) {
@@ -201,19 +217,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_load(smem + L::kSFV + s * 512, p.v_sf + (static_cast<size_t>(bh) * p.ntiles + j) * 512, 512,
                   bar_kv_full + s);
       }
+      issued = j + 1;
       __syncwarp();
     }
     // Before leaving, make sure no copy into this CTA's shared memory is
-    // still in flight: wait for the last fill of every stage.
-    for (int j = nkv - kStages < 0 ? 0 : nkv - kStages; j < nkv; ++j)
-      mbar_wait(bar_kv_full + (j % kStages), (j / kStages) & 1, abort_flag, p.status, 2);
-    mbar_wait(bar_q_full, 0, abort_flag, p.status, 3);
+    // still in flight, even when the CTA is giving up: wait for the last
+    // issued fill of every stage.
+    for (int j = issued - kStages < 0 ? 0 : issued - kStages; j < issued; ++j)
+      mbar_wait_drain(bar_kv_full + (j % kStages), (j / kStages) & 1, abort_flag, p.status, 2);
+    mbar_wait_drain(bar_q_full, 0, abort_flag, p.status, 3);
   } else if (warp == kWarpMma0 || (warp == kWarpMma0 + 1 && has1)) {
     // ------------------------------------------------------------ MMA issuers
     // Warp 9 + t issues everything of query tile t.  The whole warp runs the
     // loop and waits (so descriptors stay warp-uniform); one elected lane
     // issues each group of tcgen05 operations.
     const int t = warp - kWarpMma0;
+    const int nkv_t = t ? nkv1 : nkv0;
     const bool leader = elect_one();
     constexpr uint32_t kSwizzleQK = (D == 128) ? 4u : 6u;  // 64-B or 32-B rows
     constexpr uint32_t kSbo = 8 * L::kRowBytes;
@@ -247,10 +266,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // The score bank is free for S_t(j) once the other tile has pulled its
     // previous S into registers (tile 0, step j: tile 1's step j-1; tile 1,
-    // step j: tile 0's step j); without a second tile, once tile 0 has pulled
-    // its own previous S.
+    // step j: tile 0's step j); without a second tile -- or, causal, once
+    // tile 0 has run out of key tiles -- once this tile has pulled its own
+    // previous S.
     auto bank_free = [&](int j) {  // before S_t(j); j >= 1 for tile 0
-      if (t == 1) return wait(bar_s_free, j & 1, 12);
+      if (t == 1) {
+        if (j < nkv0) return wait(bar_s_free, j & 1, 12);
+        return wait(bar_s_free + 1, (j - 1) & 1, 16);
+      }
       return wait(bar_s_free + (has1 ? 1 : 0), (j - 1) & 1, 13);
     };
     auto issue_qk = [&](int j) {  // K scale atoms of step j, then S = Q_t K(j)^T
@@ -281,6 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_mxf4(t_l, pdesc + 2, ones_desc + 2, idesc_l1, t_sfp, t_sf1, true);
         tc_commit(o_full);
         tc_commit(bar_kv_empty + s);
+        // a stage that tile 0 does not consume still needs both releases
+        if (t == 1 && j >= nkv0) tc_commit(bar_kv_empty + s);
       }
       __syncwarp();
     };
@@ -303,8 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Per KV step j: the next scores first (they need only K(j+1) and the
     // bank), then this tile's PV product of step j.
-    for (int j = 0; ok && j < nkv; ++j) {
-      if (j + 1 < nkv) {
+    for (int j = 0; ok && j < nkv_t; ++j) {
+      if (j + 1 < nkv_t) {
         if (!(ok = wait(bar_kv_full + (j + 1) % kStages, ((j + 1) / kStages) & 1, 14))) break;
         if (!(ok = bank_free(j + 1))) break;
         tc_fence_after();
@@ -314,11 +339,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       issue_pv(j);
     }
+    // Every MMA and scale copy this warp issued must have completed before
+    // TMEM is freed, even when the CTA is giving up.
+    if (leader) tc_commit(bar_drain + t);
+    __syncwarp();
+    mbar_wait_drain(bar_drain + t, 0, abort_flag, p.status, 17);
   } else if (warp < 8 && (warp < 4 || has1)) {
     // ------------------------------------------------------------ softmax rows
     const int t = warp >> 2;            // query tile of this warpgroup
     const int row = threadIdx.x & 127;  // == TMEM lane
-    const int qrow = (qt0 + t) * 128 + row;
+    const int qrow = (t ? qt1 : qt0) * 128 + row;
+    const int nkv_t = t ? nkv1 : nkv0;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + kColS;
     const uint32_t tO = tmem + lane_base + kColO + t * D;
@@ -337,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     // tcgen05.ld / tcgen05.st are warp-collective (.sync.aligned): every
     // branch around them below is made warp-uniform with a vote.
-    for (int j = 0; j < nkv; ++j) {
+    for (int j = 0; j < nkv_t; ++j) {
       ok = mbar_wait(s_full, j & 1, abort_flag, p.status, 20);
       if (!__all_sync(0xFFFFFFFFu, ok)) {
         ok = false;
@@ -357,9 +388,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free);
 
-      const int valid = N - j * 128;  // keys of this tile that exist (>= 1)
+      int valid = N - j * 128;  // keys of this tile that exist (>= 1)
+      // causal: on the diagonal tile (the last one) row r sees keys 0 .. r
+      if (CAUSAL && j == nkv_t - 1) valid = min(valid, row + 1);
       if (valid < 128) {
-        // partial last tile: keys past N are masked and the maxima retaken
+        // partial tile: keys past N (or past the diagonal) are masked and the
+        // maxima retaken
 #pragma unroll
         for (int i = 0; i < 128; ++i)
           if (i >= valid) s[i] = -INFINITY;
@@ -466,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(p_full);
     }
     // ------------------------------------------------------------ epilogue
-    if (ok) ok = mbar_wait(o_full, (nkv - 1) & 1, abort_flag, p.status, 22);
+    if (ok) ok = mbar_wait(o_full, (nkv_t - 1) & 1, abort_flag, p.status, 22);
     if (__all_sync(0xFFFFFFFFu, ok)) {
       tc_fence_after();
       const float l = l_run + tmem_ld1(tL);
@@ -538,7 +572,7 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool DUMP>
+template <int D, bool DUMP, bool CAUSAL = false>
 int launch(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k, const fp4attn_mxfp4_t* v, void* o, float* lse,
            int B, int H, int N, float softmax_scale, int dump_bh, int row0, int nrows, uint8_t* codes,
            int32_t* kshift, float* o_f32, cudaStream_t stream, DeviceStatus* status_word = nullptr) {
@@ -578,7 +612,7 @@ int launch(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k, const fp4attn_mxf
   prm.dump_codes = codes;
   prm.dump_kshift = kshift;
   prm.dump_o = o_f32;
-  auto kern = fwd_directp_kernel<D, DUMP>;
+  auto kern = fwd_directp_kernel<D, DUMP, CAUSAL>;
   static std::once_flag attr_once[64];
   int dev = 0;
   cudaGetDevice(&dev);
@@ -587,6 +621,7 @@ int launch(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k, const fp4attn_mxf
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   });
   if (attr_err != cudaSuccess) return FP4ATTN_ERR_CUDA;
+  // two query tiles per CTA: (2c, 2c+1), or causal (c, ntiles-1-c)
   dim3 grid((ntiles + 1) / 2, BH);
   kern<<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, prm);
   return cuda_status(cudaGetLastError());
@@ -634,6 +669,59 @@ extern "C" int fp4attn_debug_dump_p(const fp4attn_nvfp4_t* q, const fp4attn_nvfp
   const int bh = b * H + h;
   if (D == 128) return launch<128, true>(q, k, v, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes, kshift, o_f32, s);
   return launch<64, true>(q, k, v, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes, kshift, o_f32, s);
+}
+
+extern "C" int fp4attn_fwd_directp_causal(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k,
+                                          const fp4attn_mxfp4_t* v, void* o, float* lse, int B, int H, int N, int D,
+                                          float softmax_scale, void* stream) {
+  const int st = check_fwd(q, k, v, o, lse, B, H, N, D, softmax_scale);
+  if (st != FP4ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (D == 128)
+    return launch<128, false, true>(q, k, v, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr, nullptr, nullptr, s);
+  return launch<64, false, true>(q, k, v, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr, nullptr, nullptr, s);
+}
+
+extern "C" int fp4attn_debug_dump_p_causal(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k,
+                                           const fp4attn_mxfp4_t* v, void* o, float* lse, int B, int H, int N, int D,
+                                           float softmax_scale, int b, int h, int row0, int nrows, uint8_t* codes,
+                                           int32_t* kshift, float* o_f32, void* stream) {
+  const int st = check_fwd(q, k, v, o, lse, B, H, N, D, softmax_scale);
+  if (st != FP4ATTN_OK) return st;
+  if (b < 0 || b >= B || h < 0 || h >= H || row0 < 0 || nrows <= 0 || row0 + nrows > N || !codes || !kshift ||
+      !o_f32 || !aligned16(codes) || !aligned16(kshift) || !aligned16(o_f32))
+    return FP4ATTN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // key tiles past a row's diagonal are never visited: their codes and
+  // shifts read as zero
+  const size_t npad = static_cast<size_t>(n_row_tiles(N)) * 128;
+  if (cudaMemsetAsync(codes, 0, static_cast<size_t>(nrows) * (npad / 2), s) != cudaSuccess ||
+      cudaMemsetAsync(kshift, 0, static_cast<size_t>(nrows) * (npad / 32) * sizeof(int32_t), s) != cudaSuccess)
+    return FP4ATTN_ERR_CUDA;
+  const int bh = b * H + h;
+  if (D == 128)
+    return launch<128, true, true>(q, k, v, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes, kshift, o_f32, s);
+  return launch<64, true, true>(q, k, v, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes, kshift, o_f32, s);
+}
+
+extern "C" int fp4attn_fwd_directp_causal_save(const void* q, const void* k, const void* v,
+                                               const fp4attn_nvfp4_buf_t* q_saved,
+                                               const fp4attn_nvfp4_buf_t* k_saved,
+                                               const fp4attn_mxfp4_buf_t* v_quant, void* o, float* lse, int B,
+                                               int H, int N, int D, float softmax_scale, void* stream) {
+  if (!q || !k || !v || !q_saved || !k_saved || !v_quant) return FP4ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return FP4ATTN_ERR_INVALID_ARG;
+  const fp4attn_nvfp4_t qn{q_saved->payload, q_saved->sf, q_saved->g};
+  const fp4attn_nvfp4_t kn{k_saved->payload, k_saved->sf, k_saved->g};
+  const fp4attn_mxfp4_t vm{v_quant->payload_t, v_quant->sf};
+  // every argument is checked before anything is launched
+  const int st = check_fwd(&qn, &kn, &vm, o, lse, B, H, N, D, softmax_scale);
+  if (st != FP4ATTN_OK) return st;
+  int r = fp4attn_quant_qk_nvfp4(q, q_saved->payload, q_saved->sf, q_saved->g, B, H, N, D, stream);
+  if (r == FP4ATTN_OK) r = fp4attn_quant_qk_nvfp4(k, k_saved->payload, k_saved->sf, k_saved->g, B, H, N, D, stream);
+  if (r == FP4ATTN_OK) r = fp4attn_quant_v_mxfp4(v, v_quant->payload_t, v_quant->sf, B, H, N, D, stream);
+  if (r == FP4ATTN_OK) r = fp4attn_fwd_directp_causal(&qn, &kn, &vm, o, lse, B, H, N, D, softmax_scale, stream);
+  return r;
 }
 
 // ------------------------------------------------------------------ allocation-free variant

@@ -73,6 +73,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Wait for asynchronous work this CTA has already issued (TMA copies into its
+// shared memory, MMAs into its TMEM) to land before the CTA leaves or frees
+// TMEM.  Unlike mbar_wait it keeps waiting when *abort is set -- the work is
+// in flight whether or not the CTA is giving up -- but it is bounded by the
+// same time limit.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                DeviceStatus* status, unsigned site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > FP4ATTN_WAIT_NS) {
+      *abort = 1;
+      if (status) {
+        if (atomicCAS(&status->timeout, 0u, 1u) == 0u) status->where = site;
+      }
+      return false;
+    }
+  }
+  return true;
+}
+
 // True in exactly one active lane of the warp (elect.sync); the warp stays
 // converged, so values computed by every lane remain warp-uniform.
 __device__ __forceinline__ bool elect_one() {

@@ -84,6 +84,19 @@ typedef struct {
     const uint8_t *sf;        /* scale atoms, fp4attn_mxfp4_v_bytes(...).sf bytes */
 } fp4attn_mxfp4_t;
 
+/* Writable buffers of a quantized NVFP4 tensor (outputs of a call). */
+typedef struct {
+    uint8_t *payload; /* [B,H,N,D/2] */
+    uint8_t *sf;      /* scale atoms, fp4attn_nvfp4_bytes(...).sf bytes */
+    float *g;         /* one fp32 tensor scale, in device memory */
+} fp4attn_nvfp4_buf_t;
+
+/* Writable buffers of a quantized MXFP4 V (outputs of a call). */
+typedef struct {
+    uint8_t *payload_t; /* [B,H,D,Npad/2] */
+    uint8_t *sf;        /* scale atoms, fp4attn_mxfp4_v_bytes(...).sf bytes */
+} fp4attn_mxfp4_buf_t;
+
 /* Message for a status code (static string, never NULL). */
 const char *fp4attn_status_string(int status);
 
@@ -119,6 +132,32 @@ int fp4attn_quant_v_mxfp4(const void *v, uint8_t *payload_t, uint8_t *sf,
 int fp4attn_fwd_directp(const fp4attn_nvfp4_t *q, const fp4attn_nvfp4_t *k, const fp4attn_mxfp4_t *v,
                         void *o, float *lse, int B, int H, int N, int D, float softmax_scale,
                         void *stream);
+
+/* Causal Direct-P forward ("What the paper found": for causal training the
+ * forward saves the quantized Q/K payloads, scales and LSE for the
+ * backward; abstract: the causal path passes the forward quantization into
+ * backward).  Query row i attends to keys 0 .. i only; otherwise it computes
+ * exactly what fp4attn_fwd_directp computes (same scale rules, mapping,
+ * denominator and LSE definition over the keys a row sees), with the same
+ * arguments, layouts and errors.  Key tiles wholly above the diagonal are
+ * skipped.  One kernel launch on stream. */
+int fp4attn_fwd_directp_causal(const fp4attn_nvfp4_t *q, const fp4attn_nvfp4_t *k, const fp4attn_mxfp4_t *v,
+                               void *o, float *lse, int B, int H, int N, int D, float softmax_scale,
+                               void *stream);
+
+/* The causal training forward in one call: NVFP4-quantizes q and k (bf16
+ * [B,H,N,D], device) into the caller's q_saved and k_saved buffers,
+ * MXFP4-quantizes v into v_quant, and runs fp4attn_fwd_directp_causal on
+ * them.  q_saved, k_saved (payloads, scale atoms, tensor scales) and lse are
+ * the state a backward pass reconstructs the probabilities from; the caller
+ * owns and keeps them.  Sizes as returned by fp4attn_nvfp4_bytes and
+ * fp4attn_mxfp4_v_bytes.  All arguments are checked before anything is
+ * launched; launches the two quantizer sequences, the V quantizer and the
+ * forward on stream. */
+int fp4attn_fwd_directp_causal_save(const void *q, const void *k, const void *v,
+                                    const fp4attn_nvfp4_buf_t *q_saved, const fp4attn_nvfp4_buf_t *k_saved,
+                                    const fp4attn_mxfp4_buf_t *v_quant, void *o, float *lse,
+                                    int B, int H, int N, int D, float softmax_scale, void *stream);
 
 /* Allocation-free variant of fp4attn_fwd_directp (the paper has no
  * counterpart; this is an interface convenience).  Some callers cannot let a
@@ -157,6 +196,15 @@ int fp4attn_debug_dump_p(const fp4attn_nvfp4_t *q, const fp4attn_nvfp4_t *k, con
                          void *o, float *lse, int B, int H, int N, int D, float softmax_scale,
                          int b, int h, int row0, int nrows, uint8_t *codes, int32_t *kshift,
                          float *o_f32, void *stream);
+
+/* fp4attn_debug_dump_p for the causal forward: the same outputs, where the
+ * codes and shifts of keys past a row's diagonal are 0.  Clears codes and
+ * kshift on stream first (the kernel never visits key tiles past the
+ * diagonal). */
+int fp4attn_debug_dump_p_causal(const fp4attn_nvfp4_t *q, const fp4attn_nvfp4_t *k, const fp4attn_mxfp4_t *v,
+                                void *o, float *lse, int B, int H, int N, int D, float softmax_scale,
+                                int b, int h, int row0, int nrows, uint8_t *codes, int32_t *kshift,
+                                float *o_f32, void *stream);
 
 /* Test support (no counterpart in the method): for format 0 (E2M1) or 1
  * (E4M3), converts every fp32 bit pattern u in [lo, hi] with the hardware

@@ -86,3 +86,32 @@ def test_argument_errors_without_gpu(L):
 def test_no_torch_types_in_header():
     src = open(HEADER).read()
     assert "torch" not in src and "at::" not in src and "Tensor" not in src
+
+
+def test_causal_argument_errors_without_gpu(L):
+    import blackwell_nvfp4_quantize_gb300 as fa
+
+    n = None
+    q = fa._NVFP4(0x1000, 0x2000, 0x3000)
+    v = fa._MXFP4(0x4000, 0x5000)
+    good = ctypes.c_void_p(0x6000)
+    args = (ctypes.byref(q), ctypes.byref(q), ctypes.byref(v), good, good, 1, 1, 128, 64)
+    assert L.fp4attn_fwd_directp_causal(*args, ctypes.c_float(float("inf")), n) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert L.fp4attn_fwd_directp_causal(ctypes.byref(q), ctypes.byref(q), ctypes.byref(v), good, good, 1, 1, 128,
+                                        48, ctypes.c_float(0.1), n) == fa.FP4ATTN_ERR_UNSUPPORTED
+    assert L.fp4attn_debug_dump_p_causal(*args, ctypes.c_float(0.1), 0, 1, 0, 8, good, good, good, n) == \
+        fa.FP4ATTN_ERR_INVALID_ARG  # h beyond H
+    # the one-call training forward checks every argument before launching
+    assert L.fp4attn_fwd_directp_causal_save(n, good, good, ctypes.byref(q), ctypes.byref(q), ctypes.byref(v),
+                                             good, good, 1, 1, 128, 64, ctypes.c_float(0.1), n) == \
+        fa.FP4ATTN_ERR_INVALID_ARG
+    assert L.fp4attn_fwd_directp_causal_save(ctypes.c_void_p(0x7001), good, good, ctypes.byref(q), ctypes.byref(q),
+                                             ctypes.byref(v), good, good, 1, 1, 128, 64, ctypes.c_float(0.1), n) == \
+        fa.FP4ATTN_ERR_INVALID_ARG
+    bad = fa._NVFP4(0x1000, 0x2000, 0)
+    assert L.fp4attn_fwd_directp_causal_save(good, good, good, ctypes.byref(q), ctypes.byref(bad), ctypes.byref(v),
+                                             good, good, 1, 1, 128, 64, ctypes.c_float(0.1), n) == \
+        fa.FP4ATTN_ERR_INVALID_ARG
+    assert L.fp4attn_fwd_directp_causal_save(good, good, good, ctypes.byref(q), ctypes.byref(q), ctypes.byref(v),
+                                             good, good, 1, 1, 128, 64, ctypes.c_float(0.0), n) == \
+        fa.FP4ATTN_ERR_INVALID_ARG
