@@ -182,9 +182,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == kWarpTma) {
+  // The only CTA on the SM holds all 512 columns, so its allocation starts at
+  // lane 0, column 0.  Addressing TMEM from the constant 0 keeps every tcgen05
+  // operand a compile-time or warp-uniform value; a different base (which the
+  // allocation rules exclude) is reported and the CTA does nothing.
+  const uint32_t tmem_base = *tmem_slot;
+  constexpr uint32_t tmem = 0;
+  if (tmem_base != 0) {
+    if (threadIdx.x == 0 && atomicCAS(&p.status->timeout, 0u, 1u) == 0u) p.status->where = 99;
+  } else if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA producer
     // The whole warp runs the loop and waits; one elected lane issues.
     const bool leader = elect_one();
@@ -229,11 +235,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMma0 || (warp == kWarpMma0 + 1 && has1)) {
     // ------------------------------------------------------------ MMA issuers
     // Warp 9 + t issues everything of query tile t.  The whole warp runs the
-    // loop and waits (so descriptors stay warp-uniform); one elected lane
-    // issues each group of tcgen05 operations.
+    // loop, waits and evaluates every operand (so they stay warp-uniform); one
+    // elected lane issues each tcgen05 operation.
     const int t = warp - kWarpMma0;
     const int nkv_t = t ? nkv1 : nkv0;
-    const bool leader = elect_one();
     constexpr uint32_t kSwizzleQK = (D == 128) ? 4u : 6u;  // 64-B or 32-B rows
     constexpr uint32_t kSbo = 8 * L::kRowBytes;
     constexpr uint32_t idesc_qk = idesc_fp4_block_scaled(128, 128, 0, 0, 0);
@@ -276,49 +281,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return wait(bar_s_free + (has1 ? 1 : 0), (j - 1) & 1, 13);
     };
+    // The whole warp runs each issue; one elected lane issues (inside the asm).
+    const uint32_t sfk_src = smem_u32(smem + L::kSFK), sfv_src = smem_u32(smem + L::kSFV);
+    const uint32_t sfp_src = smem_u32(smem + L::kSFP + t * 512);
     auto issue_qk = [&](int j) {  // K scale atoms of step j, then S = Q_t K(j)^T
       const int s = j % kStages;
       const uint32_t sfk = t_sfk + 8 * (j & 1);
-      if (leader) {
 #pragma unroll
-        for (int a = 0; a < L::kSFAtoms; ++a)
-          tc_cp_sf_atom(sfk + 4 * a, smem + L::kSFK + (s * L::kSFAtoms + a) * 512);
+      for (int a = 0; a < L::kSFAtoms; ++a) tc_cp_sf_atom_warp(sfk + 4 * a, sfk_src + (s * L::kSFAtoms + a) * 512);
 #pragma unroll
-        for (int ks = 0; ks < D / 64; ++ks)
-          mma_nvf4(t_s, qdesc + 2 * ks, kdesc0 + s * kQKStep + 2 * ks, idesc_qk, t_sfq + 4 * ks, sfk + 4 * ks,
-                   ks > 0);
-        tc_commit(s_full);
-      }
-      __syncwarp();
+      for (int ks = 0; ks < D / 64; ++ks)
+        mma_nvf4_warp(t_s, qdesc + 2 * ks, kdesc0 + s * kQKStep + 2 * ks, idesc_qk, t_sfq + 4 * ks, sfk + 4 * ks,
+                      ks > 0);
+      tc_commit_warp(s_full);
     };
     auto issue_pv = [&](int j) {  // P and V scale atoms, O_t += P_t V(j), l_t = P_t 1
       const int s = j % kStages;
       const uint32_t sfv = t_sfv + 4 * (j & 1);
       const uint64_t vd = vdesc0 + s * kVStep;
-      if (leader) {
-        tc_cp_sf_atom(t_sfp, smem + L::kSFP + t * 512);
-        tc_cp_sf_atom(sfv, smem + L::kSFV + s * 512);
-        mma_mxf4(t_o, pdesc, vd, idesc_pv0, t_sfp, sfv, j > 0);
-        mma_mxf4(t_o, pdesc + 2, vd + 2, idesc_pv1, t_sfp, sfv, true);
-        mma_mxf4(t_l, pdesc, ones_desc, idesc_l0, t_sfp, t_sf1, false);
-        mma_mxf4(t_l, pdesc + 2, ones_desc + 2, idesc_l1, t_sfp, t_sf1, true);
-        tc_commit(o_full);
-        tc_commit(bar_kv_empty + s);
-        // a stage that tile 0 does not consume still needs both releases
-        if (t == 1 && j >= nkv0) tc_commit(bar_kv_empty + s);
-      }
-      __syncwarp();
+      tc_cp_sf_atom_warp(t_sfp, sfp_src);
+      tc_cp_sf_atom_warp(sfv, sfv_src + s * 512);
+      mma_mxf4_warp(t_o, pdesc, vd, idesc_pv0, t_sfp, sfv, j > 0);
+      mma_mxf4_warp(t_o, pdesc + 2, vd + 2, idesc_pv1, t_sfp, sfv, true);
+      mma_mxf4_warp(t_l, pdesc, ones_desc, idesc_l0, t_sfp, t_sf1, false);
+      mma_mxf4_warp(t_l, pdesc + 2, ones_desc + 2, idesc_l1, t_sfp, t_sf1, true);
+      tc_commit_warp(o_full);
+      tc_commit_warp(bar_kv_empty + s);
+      // a stage that tile 0 does not consume still needs both releases
+      if (t == 1 && j >= nkv0) tc_commit_warp(bar_kv_empty + s);
     };
 
     bool ok = wait(bar_q_full, 0, 10);
     if (ok) {
       tc_fence_after();
-      if (leader) {
-        for (int a = 0; a < L::kSFAtoms; ++a)
-          tc_cp_sf_atom(t_sfq + 4 * a, smem + L::kSFQ + (t * L::kSFAtoms + a) * 512);
-        tc_cp_sf_atom(t_sf1, smem + L::kSFOnes);
-      }
-      __syncwarp();
+      for (int a = 0; a < L::kSFAtoms; ++a)
+        tc_cp_sf_atom_warp(t_sfq + 4 * a, smem_u32(smem + L::kSFQ + (t * L::kSFAtoms + a) * 512));
+      tc_cp_sf_atom_warp(t_sf1, smem_u32(smem + L::kSFOnes));
       ok = wait(bar_kv_full, 0, 11);
     }
     if (ok && t == 1) ok = wait(bar_s_free, 0, 12);  // tile 0 has pulled S_0(0)
@@ -341,8 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Every MMA and scale copy this warp issued must have completed before
     // TMEM is freed, even when the CTA is giving up.
-    if (leader) tc_commit(bar_drain + t);
-    __syncwarp();
+    tc_commit_warp(bar_drain + t);
     mbar_wait_drain(bar_drain + t, 0, abort_flag, p.status, 17);
   } else if (warp < 8 && (warp < 4 || has1)) {
     // ------------------------------------------------------------ softmax rows
@@ -543,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   if (warp == kWarpMma0) {
     __syncwarp();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
