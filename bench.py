@@ -43,9 +43,12 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic of one forward launch, from an ncu capture (see profiles/), and
 # the hash of the kernel sources it was taken on; reported only while the
 # sources are unchanged.
-TRAFFIC_RECORD = {"sources_sha": "7722b03be3aa9174", "bytes_per_launch": 278279936 + 291816448,
+TRAFFIC_RECORD = {"sources_sha": "921ec241564feee3", "bytes_per_launch": 278377984 + 291709440,
                   "note": "dram__bytes_read.sum + dram__bytes_write.sum of one launch on the 40-head "
                           "N=32768 D=128 workload (profiles/fwd_directp_B1_H40_N32768_D128_traffic.md)"}
+TRAFFIC_RECORD_CAUSAL = {"sources_sha": TRAFFIC_RECORD["sources_sha"], "bytes_per_launch": 278469632 + 292907008,
+                         "note": "the same capture of the causal forward "
+                                 "(profiles/fwd_directp_B1_H40_N32768_D128_traffic.md)"}
 KERNEL_SOURCES = ["blackwell_nvfp4_quantize_gb300/csrc/fwd_directp.cu", "blackwell_nvfp4_quantize_gb300/csrc/ptx.cuh"]
 
 
@@ -322,9 +325,8 @@ def run_ours(args, w):
     achieved = flops / (fwd_avg * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS)) * FP4_OVER_BF16
-    traffic = TRAFFIC_RECORD["bytes_per_launch"] if TRAFFIC_RECORD["sources_sha"] == sources_sha() else None
-    if args.causal:
-        traffic = None  # the recorded capture is of the noncausal forward
+    record = TRAFFIC_RECORD_CAUSAL if args.causal else TRAFFIC_RECORD
+    traffic = record["bytes_per_launch"] if record["sources_sha"] == sources_sha() else None
     line = {
         "metric": METRIC_CAUSAL if args.causal else METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
