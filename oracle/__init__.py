@@ -68,11 +68,13 @@ def _load():
     lib.orc_quant_nvfp4.restype = None
     lib.orc_quant_mxfp4_v.argtypes = [u16p, c_int, c_int, c_int, c_int, u8p, u8p, c_int]
     lib.orc_quant_mxfp4_v.restype = None
+    lib.orc_quant_mxfp8_v.argtypes = [u16p, c_int, c_int, c_int, c_int, u8p, u8p, c_int]
+    lib.orc_quant_mxfp8_v.restype = None
     lib.orc_directp_rows.argtypes = [u8p, u8p, ctypes.c_float, u8p, u8p, ctypes.c_float, u8p, u8p,
-                                     c_int, c_int, c_int, c_int, ctypes.c_float, c_int, i64p, c_int,
+                                     c_int, c_int, c_int, c_int, ctypes.c_float, c_int, c_int, i64p, c_int,
                                      f64p, f64p, u8p, i32p, i32p, c_int]
     lib.orc_directp_rows.restype = None
-    lib.orc_directp_map_row.argtypes = [f32p, c_int, ctypes.c_float, u8p, i32p, i32p, f64p]
+    lib.orc_directp_map_row.argtypes = [f32p, c_int, ctypes.c_float, c_int, u8p, i32p, i32p, f64p]
     lib.orc_directp_map_row.restype = None
     lib.orc_exact_rows.argtypes = [u16p, u16p, u16p, c_int, c_int, c_int, c_int, ctypes.c_double, c_int,
                                    i64p, c_int, f64p, f64p, c_int]
@@ -152,13 +154,32 @@ def quant_mxfp4_v(v_bf16_bits: np.ndarray, threads: int | None = None):
     return payload_t, sf
 
 
+def quant_mxfp8_v(v_bf16_bits: np.ndarray, threads: int | None = None):
+    """v: uint16 bf16 bit patterns [B,H,N,D] -> (payload_t [B,H,D,Npad] u8 E4M3 codes, sf u8)."""
+    lib = _load()
+    v = np.ascontiguousarray(v_bf16_bits, dtype=np.uint16)
+    B, H, N, D = v.shape
+    npad = (N + 127) // 128 * 128
+    payload_t = np.zeros((B, H, D, npad), dtype=np.uint8)
+    sf = np.zeros(lib.orc_mxfp4_sf_bytes(B, H, N, D), dtype=np.uint8)
+    lib.orc_quant_mxfp8_v(_ptr(v, ctypes.c_uint16), B, H, N, D, _ptr(payload_t, ctypes.c_uint8),
+                          _ptr(sf, ctypes.c_uint8), threads or default_threads())
+    return payload_t, sf
+
+
+PV_MXFP4, PV_MXFP8 = 0, 1
+
+
 # ---- attention -----------------------------------------------------------
 
-def directp_rows(q, k, v, shape, softmax_scale, rows, threads=None, want_codes=False, causal=False):
+def directp_rows(q, k, v, shape, softmax_scale, rows, threads=None, want_codes=False, causal=False,
+                 pv_fmt=PV_MXFP4):
     """Direct-P forward for selected rows.
 
-    q, k: (payload, sf, g) as returned by quant_nvfp4; v: (payload_t, sf).
-    rows: int64 flat row ids (b*H + h)*N + i.  causal: row i sees keys 0..i.
+    q, k: (payload, sf, g) as returned by quant_nvfp4; v: (payload_t, sf) from
+    quant_mxfp4_v (pv_fmt PV_MXFP4: E2M1 P and V) or quant_mxfp8_v (PV_MXFP8:
+    E4M3 P and V).  rows: int64 flat row ids (b*H + h)*N + i.  causal: row i
+    sees keys 0..i.
     Returns dict with o [R,D] f64, lse [R] f64 and, when want_codes, codes
     [R,Npad] u8 (one code per byte), kshift [R,Npad/32] i32, m [R] i32.
     """
@@ -185,7 +206,7 @@ def directp_rows(q, k, v, shape, softmax_scale, rows, threads=None, want_codes=F
         _ptr(qp, ctypes.c_uint8), _ptr(qsf, ctypes.c_uint8), float(gq),
         _ptr(kp, ctypes.c_uint8), _ptr(ksf, ctypes.c_uint8), float(gk),
         _ptr(vp, ctypes.c_uint8), _ptr(vsf, ctypes.c_uint8),
-        B, H, N, D, float(softmax_scale), int(bool(causal)), _ptr(rows, ctypes.c_int64), R,
+        B, H, N, D, float(softmax_scale), int(bool(causal)), int(pv_fmt), _ptr(rows, ctypes.c_int64), R,
         _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
         _ptr(codes, ctypes.c_uint8) if want_codes else null_u8,
         _ptr(kshift, ctypes.c_int32) if want_codes else null_i32,
@@ -194,8 +215,8 @@ def directp_rows(q, k, v, shape, softmax_scale, rows, threads=None, want_codes=F
     return out
 
 
-def directp_map_row(s: np.ndarray, c: float):
-    """One row of fp32 scores -> (codes u8[n], kshift i32[ceil(n/32)], M, l)."""
+def directp_map_row(s: np.ndarray, c: float, pv_fmt=PV_MXFP4):
+    """One row of fp32 scores -> (codes u8[n], kshift i32[ceil(n/32)], M, l); E2M1 or E4M3 codes."""
     lib = _load()
     s = np.ascontiguousarray(s, dtype=np.float32)
     n = s.shape[0]
@@ -203,7 +224,7 @@ def directp_map_row(s: np.ndarray, c: float):
     ks = np.zeros(((n + 31) // 32,), dtype=np.int32)
     m = ctypes.c_int32(0)
     l = ctypes.c_double(0.0)
-    lib.orc_directp_map_row(_ptr(s, ctypes.c_float), n, float(c), _ptr(codes, ctypes.c_uint8),
+    lib.orc_directp_map_row(_ptr(s, ctypes.c_float), n, float(c), int(pv_fmt), _ptr(codes, ctypes.c_uint8),
                             _ptr(ks, ctypes.c_int32), ctypes.byref(m), ctypes.byref(l))
     return codes, ks, int(m.value), float(l.value)
 

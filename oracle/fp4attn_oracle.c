@@ -272,6 +272,50 @@ void orc_quant_mxfp4_v(const uint16_t *v, int B, int H, int N, int D,
 }
 
 /* ------------------------------------------------------------------------ */
+/* MXFP8 quantizer (V, along keys, transposed)                              */
+/* ------------------------------------------------------------------------ */
+
+/* The same 32-key blocks and E8M0 scale atoms as MXFP4 V; the scale is the
+ * smallest power of two 2^e (e >= -127) with amax <= 448 * 2^e, and each code
+ * is E4M3(v * 2^-e), one byte per key. */
+static void mxfp8_chunk(void *p, long lo, long hi) {
+    mxfp4_ctx *c = (mxfp4_ctx *)p;
+    const int N = c->N, D = c->D, Npad = row_tiles(N) * 128;
+    for (long unit = lo; unit < hi; unit++) { /* unit = bh*D + d */
+        long bh = unit / D;
+        int d = (int)(unit % D);
+        uint8_t *prow = c->payload_t + unit * Npad;
+        for (int kb = 0; kb < Npad / 32; kb++) {
+            float amax = 0.0f;
+            for (int j = 0; j < 32; j++) {
+                int n = kb * 32 + j;
+                if (n >= N) break;
+                float a = fabsf(bf16_to_float(c->v[(bh * N + n) * D + d]));
+                if (a > amax) amax = a;
+            }
+            int e = -127;
+            while (e < 127 && (double)amax > ldexp(448.0, e)) e++;
+            size_t atom = (size_t)bh * row_tiles(N) + (size_t)(kb / 4);
+            c->sf[atom * 512 + (size_t)((d % 32) * 16 + (d / 32) * 4 + (kb % 4))] = (uint8_t)(e + 127);
+            for (int j = 0; j < 32; j++) {
+                int n = kb * 32 + j;
+                uint8_t code = 0;
+                if (n < N) code = orc_e4m3_encode(ldexp((double)bf16_to_float(c->v[(bh * N + n) * D + d]), -e));
+                prow[kb * 32 + j] = code;
+            }
+        }
+    }
+}
+
+void orc_quant_mxfp8_v(const uint16_t *v, int B, int H, int N, int D,
+                       uint8_t *payload_t, uint8_t *sf, int nthreads) {
+    assert(D <= 128);
+    mxfp4_ctx c = {v, B, H, N, D, payload_t, sf};
+    memset(sf, 0, orc_mxfp4_sf_bytes(B, H, N, D));
+    parallel_for((long)B * H * D, nthreads, mxfp8_chunk, &c);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Direct-P row mapping                                                     */
 /* ------------------------------------------------------------------------ */
 
@@ -279,6 +323,9 @@ void orc_quant_mxfp4_v(const uint16_t *v, int B, int H, int N, int D,
  * smallest integer with X_b - K_b <= log2 6, i.e. with the block's largest
  * probability 2^(X_b - K_b) within E2M1's largest finite value 6. */
 static const float LOG2_6_F32 = 2.5849625007211561f;
+/* log2(448) rounded to fp32: the same rule for E4M3 probability codes, whose
+ * largest finite value is 448. */
+static const float LOG2_448_F32 = 8.8073549220576041f;
 
 /* 2^t for an fp32 t, in fp64: exact for integers, correctly rounded libm
  * otherwise (the decision it feeds is taken against irrational thresholds). */
@@ -287,10 +334,12 @@ static double exp2_exact(float t) {
     return exp2((double)t);
 }
 
-/* One row: scores s[0..n), multiplier c.  Returns codes, K_b, M and l. */
-void orc_directp_map_row(const float *s, int n, float c,
+/* One row: scores s[0..n), multiplier c, code format fmt (ORC_PV_MXFP4:
+ * E2M1, ORC_PV_MXFP8: E4M3).  Returns codes, K_b, M and l. */
+void orc_directp_map_row(const float *s, int n, float c, int fmt,
                          uint8_t *codes, int32_t *kshift, int32_t *m_out,
                          double *l_out) {
+    const float log2_max = (fmt == ORC_PV_MXFP8) ? LOG2_448_F32 : LOG2_6_F32;
     int nblk = (n + 31) / 32;
     float xmax = -INFINITY;
     for (int j = 0; j < n; j++) {
@@ -306,16 +355,17 @@ void orc_directp_map_row(const float *s, int n, float c,
             float x = c * s[j];
             if (x > xb) xb = x;
         }
-        int32_t K = (int32_t)ceilf(xb - LOG2_6_F32);
+        int32_t K = (int32_t)ceilf(xb - log2_max);
         kshift[b] = K;
         int e = K - M;
         if (e < -127) e = -127;
         double scale = ldexp(1.0, e);
         for (int j = j0; j < j1; j++) {
             float t = fmaf(c, s[j], (float)(-K));
-            uint8_t code = orc_e2m1_encode(exp2_exact(t));
+            double p = exp2_exact(t);
+            uint8_t code = (fmt == ORC_PV_MXFP8) ? orc_e4m3_encode(p) : orc_e2m1_encode(p);
             codes[j] = code;
-            l += orc_e2m1_decode(code) * scale;
+            l += ((fmt == ORC_PV_MXFP8) ? orc_e4m3_decode(code) : orc_e2m1_decode(code)) * scale;
         }
     }
     *m_out = M;
@@ -335,6 +385,7 @@ typedef struct {
     float gq, gk, c;
     int B, H, N, D;
     int causal; /* row i sees keys 0..i only */
+    int pv_fmt; /* ORC_PV_MXFP4 or ORC_PV_MXFP8 */
     /* per-head decoded operands */
     long bh;
     double *khat; /* [N][D] */
@@ -360,13 +411,18 @@ static void decode_head_chunk(void *p, long lo, long hi) {
             a->khat[n * D + d] = orc_e2m1_decode(code) * orc_e4m3_decode(sfb);
         }
         for (int d = 0; d < D; d++) {
-            const uint8_t *vr = a->vp + ((size_t)a->bh * D + (size_t)d) * (Npad / 2);
-            uint8_t byte = vr[n / 2];
-            uint8_t code = (n % 2 == 0) ? (byte & 0xF) : (byte >> 4);
             size_t atom = (size_t)a->bh * row_tiles(N) + (size_t)(n / 128);
             int kb = (int)((n % 128) / 32);
             uint8_t sfb = a->vsf[atom * 512 + (size_t)((d % 32) * 16 + (d / 32) * 4 + kb)];
-            a->vhat[n * D + d] = orc_e2m1_decode(code) * orc_e8m0_decode(sfb);
+            if (a->pv_fmt == ORC_PV_MXFP8) {
+                const uint8_t *vr = a->vp + ((size_t)a->bh * D + (size_t)d) * Npad;
+                a->vhat[n * D + d] = orc_e4m3_decode(vr[n]) * orc_e8m0_decode(sfb);
+            } else {
+                const uint8_t *vr = a->vp + ((size_t)a->bh * D + (size_t)d) * (Npad / 2);
+                uint8_t byte = vr[n / 2];
+                uint8_t code = (n % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+                a->vhat[n * D + d] = orc_e2m1_decode(code) * orc_e8m0_decode(sfb);
+            }
         }
     }
 }
@@ -401,12 +457,13 @@ static void attn_rows_chunk(void *p, long lo, long hi) {
         memset(ks, 0, sizeof(int32_t) * (size_t)(Npad / 32));
         int32_t M;
         double l;
-        orc_directp_map_row(s32, nk, a->c, codes, ks, &M, &l);
+        orc_directp_map_row(s32, nk, a->c, a->pv_fmt, codes, ks, &M, &l);
         for (int d = 0; d < D; d++) acc[d] = 0.0;
         for (int j = 0; j < nk; j++) {
             int e = ks[j / 32] - M;
             if (e < -127) e = -127;
-            double pj = orc_e2m1_decode(codes[j]) * ldexp(1.0, e);
+            double dec = (a->pv_fmt == ORC_PV_MXFP8) ? orc_e4m3_decode(codes[j]) : orc_e2m1_decode(codes[j]);
+            double pj = dec * ldexp(1.0, e);
             if (pj == 0.0) continue;
             for (int d = 0; d < D; d++) acc[d] += pj * a->vhat[(size_t)j * D + d];
         }
@@ -426,7 +483,7 @@ static void attn_rows_chunk(void *p, long lo, long hi) {
 void orc_directp_rows(const uint8_t *q_payload, const uint8_t *q_sf, float g_q,
                       const uint8_t *k_payload, const uint8_t *k_sf, float g_k,
                       const uint8_t *v_payload_t, const uint8_t *v_sf,
-                      int B, int H, int N, int D, float softmax_scale, int causal,
+                      int B, int H, int N, int D, float softmax_scale, int causal, int pv_fmt,
                       const int64_t *rows, int nrows,
                       double *o, double *lse,
                       uint8_t *codes, int32_t *kshift, int32_t *mrow,
@@ -446,6 +503,7 @@ void orc_directp_rows(const uint8_t *q_payload, const uint8_t *q_sf, float g_q,
     a.N = N;
     a.D = D;
     a.causal = causal;
+    a.pv_fmt = pv_fmt;
     /* the log2-domain score multiplier, rounded once to fp32 */
     a.c = (float)((((double)softmax_scale * LOG2E) * (double)g_q) * (double)g_k);
     a.rows = rows;

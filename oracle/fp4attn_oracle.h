@@ -88,6 +88,19 @@ size_t orc_mxfp4_sf_bytes(int B, int H, int N, int D);
 void orc_quant_mxfp4_v(const uint16_t *v, int B, int H, int N, int D,
                        uint8_t *payload_t, uint8_t *sf, int nthreads);
 
+/* MXFP8 for V along the key axis, written transposed (the FP8 P/V variant:
+ * "What the paper found", training keeps FP8 probabilities and values).
+ *   per (b,h,d) and 32-key block:  e = the smallest integer >= -127 with
+ *   amax <= 448 * 2^e;  scale byte e+127;  code = E4M3( v * 2^-e ).
+ * payload: [B,H,D,Npad] bytes (one code per key), padded keys 0.
+ * sf     : atoms exactly as for MXFP4 V (size orc_mxfp4_sf_bytes).
+ * Pinned: hand-worked block, amax <= 448*2^e < 2*amax, error bound. */
+void orc_quant_mxfp8_v(const uint16_t *v, int B, int H, int N, int D,
+                       uint8_t *payload_t, uint8_t *sf, int nthreads);
+
+/* P/V operand formats of the PV product. */
+enum { ORC_PV_MXFP4 = 0, ORC_PV_MXFP8 = 1 };
+
 /* ---- Direct-P attention, two-pass restatement ----
  * For each requested row i of head bh (rows[r] = bh*N + i), over the keys j
  * the row sees -- all N, or with causal != 0 ("What the paper found": the
@@ -95,10 +108,12 @@ void orc_quant_mxfp4_v(const uint16_t *v, int B, int H, int N, int D,
  *   S_ij   = sum_d qhat_id * khat_jd                    (fp64, exact here)
  *   c      = fp32( softmax_scale * log2(e) * g_Q * g_K ) (fp64 products)
  *   X_ij   = fp32( c * fp32(S_ij) )
- *   X_b    = max of X over each 32-key block,  K_b = ceil(X_b - log2 6)
+ *   X_b    = max of X over each 32-key block,  K_b = ceil(X_b - log2 R)
+ *            with R the largest finite code value: 6 (E2M1, pv_fmt
+ *            ORC_PV_MXFP4) or 448 (E4M3, pv_fmt ORC_PV_MXFP8)
  *   M_i    = ceil(max_j X_ij)                      (an integer row max)
  *   t_ij   = fmaf(c, fp32(S_ij), -K_b)
- *   code   = E2M1( 2^t_ij )                         (exact exponential)
+ *   code   = E2M1 or E4M3 ( 2^t_ij )                (exact exponential)
  *   e_b    = max(K_b - M_i, -127),  p_ij = dec(code) * 2^e_b
  *   l_i    = sum_j p_ij,  O_i = sum_j p_ij vhat_j / l_i,
  *   LSE_i  = ln2 * (M_i + log2 l_i)
@@ -112,17 +127,17 @@ void orc_quant_mxfp4_v(const uint16_t *v, int B, int H, int N, int D,
 void orc_directp_rows(const uint8_t *q_payload, const uint8_t *q_sf, float g_q,
                       const uint8_t *k_payload, const uint8_t *k_sf, float g_k,
                       const uint8_t *v_payload_t, const uint8_t *v_sf,
-                      int B, int H, int N, int D, float softmax_scale, int causal,
+                      int B, int H, int N, int D, float softmax_scale, int causal, int pv_fmt,
                       const int64_t *rows, int nrows,
                       double *o, double *lse,
                       uint8_t *codes, int32_t *kshift, int32_t *mrow,
                       int nthreads);
 
-/* The same row pass on explicit scores: for one row of n fp32 scores S and
- * multiplier c, returns the codes (n bytes), K_b per 32-key block, M and l
- * (with p = dec(code)*2^e_b as above).  Used to pin the mapping on
- * hand-worked rows. */
-void orc_directp_map_row(const float *s, int n, float c,
+/* The same row pass on explicit scores: for one row of n fp32 scores S,
+ * multiplier c and code format fmt, returns the codes (n bytes), K_b per
+ * 32-key block, M and l (with p = dec(code)*2^e_b as above).  Used to pin the
+ * mapping on hand-worked rows. */
+void orc_directp_map_row(const float *s, int n, float c, int fmt,
                          uint8_t *codes, int32_t *kshift, int32_t *m_out,
                          double *l_out);
 
