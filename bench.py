@@ -18,6 +18,7 @@ no flush is needed between steps.
 tests) on a bounded sample of the same workload; it is a reported baseline.
 --causal times the causal forward instead (query i sees keys 0..i); its
 FLOPs are counted over the unmasked (query, key) pairs, 4*D*N*(N+1)/2 per head.
+--fp8pv times the FP8 P/V variant (MXFP8 V, E4M3 probability codes).
 """
 from __future__ import annotations
 
@@ -35,9 +36,18 @@ sys.path.insert(0, ROOT)
 
 METRIC = "Direct-P FP4 attn fwd TFLOP/s (4BHN²D/t), % of GB300 dense FP4 peak"
 METRIC_CAUSAL = "Causal Direct-P FP4 attn fwd TFLOP/s (4BHD·N(N+1)/2 / t), % of GB300 dense FP4 peak"
+
+
+def metric_name(args):
+    m = METRIC_CAUSAL if args.causal else METRIC
+    return m.replace("FP4 attn", "FP4-QK/FP8-PV attn") if args.fp8pv else m
 UNIT = "TFLOP/s"
 # Dense FP4 : dense BF16 tensor throughput on GB300, nominal 13.5 : 2.25 PFLOP/s.
 FP4_OVER_BF16 = 13.5 / 2.25
+# FP8 P/V variant: QK^T (half the FLOPs) on FP4 operands, PV (the other half)
+# on FP8 operands at 4.5 : 2.25 of the BF16 rate -- the two halves take time in
+# sequence, so the combined peak is their harmonic combination.
+FP8PV_OVER_BF16 = 1.0 / (0.5 / FP4_OVER_BF16 + 0.5 / (4.5 / 2.25))
 FALLBACK_BF16_TFLOPS = 1900.0
 
 # DRAM traffic of one forward launch, from an ncu capture (see profiles/), and
@@ -134,7 +144,7 @@ def attn_flops(rows, N, D, causal):
     return 4.0 * D * float(keys)
 
 
-def cpu_baseline(w, q, k, v, causal=False, budget_s=12.0):
+def cpu_baseline(w, q, k, v, causal=False, fp8pv=False, budget_s=12.0):
     """The oracle as it stands, on host cores, on a bounded row sample of head 0."""
     import numpy as np
 
@@ -151,17 +161,18 @@ def cpu_baseline(w, q, k, v, causal=False, budget_s=12.0):
     t0 = time.perf_counter()
     qq = oracle.quant_nvfp4(qb, threads)
     kq = oracle.quant_nvfp4(kb, threads)
-    vq = oracle.quant_mxfp4_v(vb, threads)
+    vq = oracle.quant_mxfp8_v(vb, threads) if fp8pv else oracle.quant_mxfp4_v(vb, threads)
+    pv_fmt = oracle.PV_MXFP8 if fp8pv else oracle.PV_MXFP4
     t_quant = time.perf_counter() - t0
     # calibrate, then time a sample sized to the budget
     probe = np.linspace(0, N - 1, min(N, 2 * threads)).astype(np.int64)
     t0 = time.perf_counter()
-    oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, probe, threads, causal=causal)
+    oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, probe, threads, causal=causal, pv_fmt=pv_fmt)
     t_probe = time.perf_counter() - t0
     rows = int(max(len(probe), min(N, len(probe) * budget_s / max(t_probe, 1e-6))))
     sample = np.linspace(0, N - 1, rows).astype(np.int64)
     t0 = time.perf_counter()
-    oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, sample, threads, causal=causal)
+    oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, sample, threads, causal=causal, pv_fmt=pv_fmt)
     t = time.perf_counter() - t0
     flops = attn_flops(sample, N, D, causal)
     return {"value": flops / t / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -184,12 +195,14 @@ def run_reference(args, w):
     B, H, N, D = w.shape
     qb, kb, vb = (wl.bf16_bits(t[:1, :1].contiguous()) for t in (q, k, v))
     shape1 = (1, 1, N, D)
-    qq, kq, vq = oracle.quant_nvfp4(qb, threads), oracle.quant_nvfp4(kb, threads), oracle.quant_mxfp4_v(vb, threads)
+    qq, kq = oracle.quant_nvfp4(qb, threads), oracle.quant_nvfp4(kb, threads)
+    vq = oracle.quant_mxfp8_v(vb, threads) if args.fp8pv else oracle.quant_mxfp4_v(vb, threads)
+    pv_fmt = oracle.PV_MXFP8 if args.fp8pv else oracle.PV_MXFP4
     causal = args.causal
     rows_per_step = max(threads, 2 * threads)
     probe = np.linspace(0, N - 1, rows_per_step).astype(np.int64)
     t0 = time.perf_counter()
-    oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, probe, threads, causal=causal)
+    oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, probe, threads, causal=causal, pv_fmt=pv_fmt)
     t_probe = time.perf_counter() - t0
     per_step_budget = max(0.5, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
     rows_per_step = int(max(threads, min(N, rows_per_step * per_step_budget / max(t_probe, 1e-6))))
@@ -199,7 +212,7 @@ def run_reference(args, w):
     for i in range(args.warmup + args.steps):
         rows = np.sort(rng.choice(N, size=rows_per_step, replace=False)).astype(np.int64)
         t0 = time.perf_counter()
-        oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, rows, threads, causal=causal)
+        oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, rows, threads, causal=causal, pv_fmt=pv_fmt)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(dt)
@@ -207,12 +220,12 @@ def run_reference(args, w):
     t = sum(times)
     value = flops / t / 1e12
     sample = "%d query rows per step of head 0 of %s (attention rows; quantization excluded)" % (rows_per_step, w.name)
-    line = {"metric": METRIC_CAUSAL if causal else METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+    line = {"metric": metric_name(args), "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * t / len(times), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "recipe": w.description,
-                       "mask": "causal" if causal else "none"},
+                       "mask": "causal" if causal else "none", "pv": "fp8" if args.fp8pv else "fp4"},
             "impl": "reference",
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -241,18 +254,24 @@ def run_ours(args, w):
 
     q_h, k_h, v_h = wl.make_inputs(w, seed=w.seed + rank)
     q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
-    qq, kq, vq = fa.empty_nvfp4(w.shape, dev), fa.empty_nvfp4(w.shape, dev), fa.empty_mxfp4(w.shape, dev)
+    qq, kq = fa.empty_nvfp4(w.shape, dev), fa.empty_nvfp4(w.shape, dev)
+    vq = fa.empty_mxfp8(w.shape, dev) if args.fp8pv else fa.empty_mxfp4(w.shape, dev)
+    quant_v = fa.quant_v_mxfp8 if args.fp8pv else fa.quant_v_mxfp4
     o = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     launches_per_step = 3 + 3 + 1 + 1  # amax, quant, finalize (x2), V quant, forward
-    fwd = fa.fwd_directp_causal if args.causal else fa.fwd_directp
+    if args.fp8pv:
+        def fwd(qq, kq, vq, scale, o, lse, stream):
+            return fa.fwd_directp_fp8pv(qq, kq, vq, scale, causal=args.causal, o=o, lse=lse, stream=stream)
+    else:
+        fwd = fa.fwd_directp_causal if args.causal else fa.fwd_directp
 
     fwd_events = []
 
     def step(record=False):
         fa.quant_qk_nvfp4(q, out=qq, stream=stream)
         fa.quant_qk_nvfp4(k, out=kq, stream=stream)
-        fa.quant_v_mxfp4(v, out=vq, stream=stream)
+        quant_v(v, out=vq, stream=stream)
         if record:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -297,7 +316,7 @@ def run_ours(args, w):
         v.copy_(v_p, non_blocking=True)
         fa.quant_qk_nvfp4(q, out=qq, stream=stream)
         fa.quant_qk_nvfp4(k, out=kq, stream=stream)
-        fa.quant_v_mxfp4(v, out=vq, stream=stream)
+        quant_v(v, out=vq, stream=stream)
         fwd(qq, kq, vq, w.softmax_scale, o=o, lse=lse, stream=stream)
         o_p.copy_(o, non_blocking=True)
         lse_p.copy_(lse, non_blocking=True)
@@ -324,32 +343,35 @@ def run_ours(args, w):
     fwd_avg = sum(fwd_ms) / len(fwd_ms)
     achieved = flops / (fwd_avg * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
-    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS)) * FP4_OVER_BF16
+    ratio = FP8PV_OVER_BF16 if args.fp8pv else FP4_OVER_BF16
+    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS)) * ratio
     record = TRAFFIC_RECORD_CAUSAL if args.causal else TRAFFIC_RECORD
-    traffic = record["bytes_per_launch"] if record["sources_sha"] == sources_sha() else None
+    traffic = record["bytes_per_launch"] if record["sources_sha"] == sources_sha() and not args.fp8pv else None
     line = {
-        "metric": METRIC_CAUSAL if args.causal else METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": metric_name(args), "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e2m1", "data": "synthetic",
+        "vs_baseline": None, "dtype": "e2m1+e4m3" if args.fp8pv else "e2m1", "data": "synthetic",
         "config": {"workload": w.name, "B": B, "H": H, "N": N, "D": D, "recipe": w.description,
-                   "step": "NVFP4 quantize Q and K, MXFP4 quantize V, %sDirect-P forward"
-                           % ("causal " if args.causal else ""),
-                   "mask": "causal" if args.causal else "none",
+                   "step": "NVFP4 quantize Q and K, %s quantize V, %sDirect-P forward"
+                           % ("MXFP8" if args.fp8pv else "MXFP4", "causal " if args.causal else ""),
+                   "mask": "causal" if args.causal else "none", "pv": "fp8" if args.fp8pv else "fp4",
                    "l2": "inputs larger than L2 (1 GB bf16 in, 0.6 GB quantized); no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "fwd_ms": fwd_avg,
         "fwd_frac_of_fp4_peak": achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": "%s bf16 dense x %.1f (nominal FP4:BF16 dense ratio), burst" % (peak_src, FP4_OVER_BF16),
-                     "kernel": "fwd_directp_kernel<%d, causal=%s>" % (D, str(bool(args.causal)).lower())},
+                     "peak_source": ("%s bf16 dense x %.1f (nominal %s dense ratio), burst"
+                                     % (peak_src, ratio, "FP4-QK/FP8-PV:BF16" if args.fp8pv else "FP4:BF16")),
+                     "kernel": "fwd_directp_kernel<%d, causal=%s, fp8pv=%s>"
+                               % (D, str(bool(args.causal)).lower(), str(bool(args.fp8pv)).lower())},
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": 3 * B * H * N * D * 2, "d2h_bytes_per_step": B * H * N * D * 2 + B * H * N * 4},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, q_h, k_h, v_h, causal=args.causal)
+        line["cpu_baseline"] = cpu_baseline(w, q_h, k_h, v_h, causal=args.causal, fp8pv=args.fp8pv)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -366,6 +388,7 @@ def main(argv=None):
     ap.add_argument("--workload", type=int, default=4, help="workload index 1-5 (default 4)")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--causal", action="store_true", help="time the causal forward (query i sees keys 0..i)")
+    ap.add_argument("--fp8pv", action="store_true", help="time the FP8 P/V variant (MXFP8 V, E4M3 codes)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -8,8 +8,9 @@ raises if the library has not been built -- there is no fallback.
 Method: "Hardware-Aware FP4 FlashAttention-4" (Direct-P for noncausal
 inference): NVFP4 Q/K, MXFP4 V along keys, scores mapped directly to MXFP4
 E2M1 probability codes, denominator from the same rounded probabilities, O
-and LSE as outputs; and its causal training forward, which keeps the
-quantized Q/K and the LSE for a backward pass.
+and LSE as outputs; its causal training forward, which keeps the quantized
+Q/K and the LSE for a backward pass; and the FP8 P/V variant (E4M3
+probability codes, MXFP8 V) kept for training.
 """
 from __future__ import annotations
 
@@ -74,7 +75,15 @@ def lib():
     L.fp4attn_debug_dump_p_causal.argtypes = L.fp4attn_debug_dump_p.argtypes
     L.fp4attn_fwd_directp_causal_save.argtypes = [vp, vp, vp, ctypes.POINTER(_NVFP4), ctypes.POINTER(_NVFP4),
                                                   ctypes.POINTER(_MXFP4), vp, vp, i, i, i, i, f, vp]
-    for name in ("fp4attn_fwd_directp_causal", "fp4attn_debug_dump_p_causal", "fp4attn_fwd_directp_causal_save",
+    L.fp4attn_mxfp8_v_bytes.argtypes = [i, i, i, i, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+    L.fp4attn_quant_v_mxfp8.argtypes = [vp, vp, vp, i, i, i, i, vp]
+    L.fp4attn_fwd_directp_fp8pv.argtypes = [ctypes.POINTER(_NVFP4), ctypes.POINTER(_NVFP4), ctypes.POINTER(_MXFP4),
+                                            vp, vp, i, i, i, i, f, i, vp]
+    L.fp4attn_debug_dump_p_fp8pv.argtypes = [ctypes.POINTER(_NVFP4), ctypes.POINTER(_NVFP4),
+                                             ctypes.POINTER(_MXFP4), vp, vp, i, i, i, i, f, i, i, i, i, i, vp, vp,
+                                             vp, vp]
+    for name in ("fp4attn_mxfp8_v_bytes", "fp4attn_quant_v_mxfp8", "fp4attn_fwd_directp_fp8pv",
+                 "fp4attn_debug_dump_p_fp8pv", "fp4attn_fwd_directp_causal", "fp4attn_debug_dump_p_causal", "fp4attn_fwd_directp_causal_save",
                  "fp4attn_fwd_directp_noalloc", "fp4attn_debug_cvt_transitions", "fp4attn_nvfp4_bytes", "fp4attn_mxfp4_v_bytes", "fp4attn_quant_qk_nvfp4",
                  "fp4attn_quant_v_mxfp4", "fp4attn_fwd_directp", "fp4attn_debug_dump_p",
                  "fp4attn_device_status"):
@@ -127,6 +136,17 @@ class MXFP4Tensor:
         return _MXFP4(self.payload_t.data_ptr(), self.sf.data_ptr())
 
 
+@dataclass
+class MXFP8Tensor:
+    """V in MXFP8 along keys (FP8 P/V variant): payload_t [B,H,D,Npad] u8 E4M3 codes, scale atoms u8."""
+    payload_t: torch.Tensor
+    sf: torch.Tensor
+    shape: tuple
+
+    def _c(self):  # same two pointers as the MXFP4 struct
+        return _MXFP4(self.payload_t.data_ptr(), self.sf.data_ptr())
+
+
 def nvfp4_bytes(B, H, N, D):
     p, s = ctypes.c_size_t(), ctypes.c_size_t()
     _check(lib().fp4attn_nvfp4_bytes(B, H, N, D, ctypes.byref(p), ctypes.byref(s)), "fp4attn_nvfp4_bytes")
@@ -136,6 +156,12 @@ def nvfp4_bytes(B, H, N, D):
 def mxfp4_v_bytes(B, H, N, D):
     p, s = ctypes.c_size_t(), ctypes.c_size_t()
     _check(lib().fp4attn_mxfp4_v_bytes(B, H, N, D, ctypes.byref(p), ctypes.byref(s)), "fp4attn_mxfp4_v_bytes")
+    return p.value, s.value
+
+
+def mxfp8_v_bytes(B, H, N, D):
+    p, s = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().fp4attn_mxfp8_v_bytes(B, H, N, D, ctypes.byref(p), ctypes.byref(s)), "fp4attn_mxfp8_v_bytes")
     return p.value, s.value
 
 
@@ -160,6 +186,14 @@ def empty_mxfp4(shape, device) -> MXFP4Tensor:
                        torch.empty((sb,), dtype=torch.uint8, device=device), tuple(shape))
 
 
+def empty_mxfp8(shape, device) -> MXFP8Tensor:
+    B, H, N, D = shape
+    pb, sb = mxfp8_v_bytes(B, H, N, D)
+    npad = (N + 127) // 128 * 128
+    return MXFP8Tensor(torch.empty((B, H, D, npad), dtype=torch.uint8, device=device),
+                       torch.empty((sb,), dtype=torch.uint8, device=device), tuple(shape))
+
+
 def quant_qk_nvfp4(x: torch.Tensor, out: NVFP4Tensor | None = None, stream=None) -> NVFP4Tensor:
     """fp4attn_quant_qk_nvfp4 on a CUDA bf16 [B,H,N,D] tensor."""
     _check_input(x, "x")
@@ -178,6 +212,33 @@ def quant_v_mxfp4(v: torch.Tensor, out: MXFP4Tensor | None = None, stream=None) 
     _check(lib().fp4attn_quant_v_mxfp4(_ptr(v), _ptr(out.payload_t), _ptr(out.sf), B, H, N, D,
                                        ctypes.c_void_p(_stream(stream))), "fp4attn_quant_v_mxfp4")
     return out
+
+
+def quant_v_mxfp8(v: torch.Tensor, out: MXFP8Tensor | None = None, stream=None) -> MXFP8Tensor:
+    """fp4attn_quant_v_mxfp8 on a CUDA bf16 [B,H,N,D] tensor (FP8 P/V variant)."""
+    _check_input(v, "v")
+    B, H, N, D = v.shape
+    out = out or empty_mxfp8(v.shape, v.device)
+    _check(lib().fp4attn_quant_v_mxfp8(_ptr(v), _ptr(out.payload_t), _ptr(out.sf), B, H, N, D,
+                                       ctypes.c_void_p(_stream(stream))), "fp4attn_quant_v_mxfp8")
+    return out
+
+
+def fwd_directp_fp8pv(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP8Tensor, softmax_scale: float | None = None,
+                      causal: bool = False, o: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                      stream=None):
+    """fp4attn_fwd_directp_fp8pv: Direct-P with E4M3 probability codes and MXFP8 V; (O, LSE)."""
+    B, H, N, D = q.shape
+    dev = q.payload.device
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    o = o if o is not None else torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev)
+    lse = lse if lse is not None else torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    qc, kc, vc = q._c(), k._c(), v._c()
+    _check(lib().fp4attn_fwd_directp_fp8pv(ctypes.byref(qc), ctypes.byref(kc), ctypes.byref(vc), _ptr(o),
+                                           _ptr(lse), B, H, N, D, float(softmax_scale), int(bool(causal)),
+                                           ctypes.c_void_p(_stream(stream))), "fp4attn_fwd_directp_fp8pv")
+    return o, lse
 
 
 def _fwd(name, q, k, v, softmax_scale, o, lse, stream):
@@ -245,10 +306,11 @@ def fwd_directp_noalloc(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP4Tensor, o: torch
     return o, lse
 
 
-def debug_dump_p(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP4Tensor, b: int, h: int, row0: int, nrows: int,
+def debug_dump_p(q: NVFP4Tensor, k: NVFP4Tensor, v, b: int, h: int, row0: int, nrows: int,
                  softmax_scale: float | None = None, stream=None, causal: bool = False):
-    """fp4attn_debug_dump_p (or fp4attn_debug_dump_p_causal): (O, LSE, codes [nrows, Npad/2] u8,
-    kshift [nrows, Npad/32] i32, O of the dumped rows in fp32 [nrows, D])."""
+    """fp4attn_debug_dump_p (or fp4attn_debug_dump_p_causal; with an MXFP8Tensor v,
+    fp4attn_debug_dump_p_fp8pv): (O, LSE, codes [nrows, Npad/2] u8 -- [nrows, Npad] E4M3 bytes
+    for FP8 P/V --, kshift [nrows, Npad/32] i32, O of the dumped rows in fp32 [nrows, D])."""
     B, H, N, D = q.shape
     dev = q.payload.device
     if softmax_scale is None:
@@ -256,10 +318,17 @@ def debug_dump_p(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP4Tensor, b: int, h: int,
     npad = (N + 127) // 128 * 128
     o = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    codes = torch.zeros((nrows, npad // 2), dtype=torch.uint8, device=dev)
+    fp8 = isinstance(v, MXFP8Tensor)
+    codes = torch.zeros((nrows, npad if fp8 else npad // 2), dtype=torch.uint8, device=dev)
     kshift = torch.zeros((nrows, npad // 32), dtype=torch.int32, device=dev)
     o32 = torch.zeros((nrows, D), dtype=torch.float32, device=dev)
     qc, kc, vc = q._c(), k._c(), v._c()
+    if fp8:
+        _check(lib().fp4attn_debug_dump_p_fp8pv(ctypes.byref(qc), ctypes.byref(kc), ctypes.byref(vc), _ptr(o),
+                                                _ptr(lse), B, H, N, D, float(softmax_scale), int(bool(causal)), b, h,
+                                                row0, nrows, _ptr(codes), _ptr(kshift), _ptr(o32),
+                                                ctypes.c_void_p(_stream(stream))), "fp4attn_debug_dump_p_fp8pv")
+        return o, lse, codes, kshift, o32
     name = "fp4attn_debug_dump_p_causal" if causal else "fp4attn_debug_dump_p"
     _check(getattr(lib(), name)(ctypes.byref(qc), ctypes.byref(kc), ctypes.byref(vc), _ptr(o), _ptr(lse),
                                 B, H, N, D, float(softmax_scale), b, h, row0, nrows, _ptr(codes),
@@ -286,10 +355,12 @@ def debug_cvt_transitions(fmt: int, lo: int, hi: int, capacity: int = 4096, stre
 
 
 def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scale: float | None = None, stream=None,
-              causal: bool = False):
-    """Quantize Q, K (NVFP4) and V (MXFP4) and run the Direct-P forward: (O, LSE)."""
+              causal: bool = False, fp8pv: bool = False):
+    """Quantize Q, K (NVFP4) and V (MXFP4, or MXFP8 with fp8pv) and run the Direct-P forward: (O, LSE)."""
     qq = quant_qk_nvfp4(q, stream=stream)
     kq = quant_qk_nvfp4(k, stream=stream)
+    if fp8pv:
+        return fwd_directp_fp8pv(qq, kq, quant_v_mxfp8(v, stream=stream), softmax_scale, causal=causal, stream=stream)
     vq = quant_v_mxfp4(v, stream=stream)
     fwd = fwd_directp_causal if causal else fwd_directp
     return fwd(qq, kq, vq, softmax_scale, stream=stream)

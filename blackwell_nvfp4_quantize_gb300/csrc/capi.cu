@@ -73,6 +73,15 @@ extern "C" int fp4attn_mxfp4_v_bytes(int B, int H, int N, int D, size_t* payload
   return FP4ATTN_OK;
 }
 
+extern "C" int fp4attn_mxfp8_v_bytes(int B, int H, int N, int D, size_t* payload_bytes, size_t* sf_bytes) {
+  const int st = check_shape(B, H, N, D);
+  if (st != FP4ATTN_OK) return st;
+  if (!payload_bytes || !sf_bytes) return FP4ATTN_ERR_INVALID_ARG;
+  *payload_bytes = mxfp8_payload_bytes(B, H, N, D);
+  *sf_bytes = mxfp4_sf_bytes(B, H, N, D);  // the same atoms
+  return FP4ATTN_OK;
+}
+
 extern "C" int fp4attn_device_status(void* stream) {
   DeviceStatus* d = device_status_ptr();
   if (!d) return FP4ATTN_ERR_CUDA;

@@ -65,24 +65,29 @@ constexpr uint32_t kColSFOnes = 488;  // tile t unit scales of the ones tile at 
 static_assert(kColSFOnes + 8 <= kTmemCols, "TMEM plan exceeds 512 columns");
 constexpr uint32_t kLN = 16;                     // N of the denominator MMA
 constexpr float kLog2Six = 2.5849625007211561f;  // log2(6) rounded to fp32
+constexpr float kLog2_448 = 8.8073549220576041f;  // log2(448) rounded to fp32 (E4M3 codes)
 constexpr double kLog2E = 1.4426950408889634074;
 // The reference maximum M of a row moves (and O, l are rescaled by an exact
 // power of two) only when a tile's ceil(max score) exceeds it by more than
 // this many binades; until then probabilities may exceed 1 by up to 2^8.
 constexpr int kRescaleSlack = 8;
 
-template <int D>
+// P8: the FP8 P/V variant -- E4M3 probability codes and MXFP8 V, one byte
+// per key, so V, P and the ones tile take twice the bytes of the E2M1 form.
+template <int D, bool P8 = false>
 struct Layout {
   static constexpr int kRowBytes = D / 2;  // packed E2M1 bytes per Q/K row
   static constexpr int kTileQK = 128 * kRowBytes;
-  static constexpr int kTileV = D * 64;    // D channels x 128 keys
-  static constexpr int kSFAtoms = D / 64;  // NVFP4 scale atoms per 128-row tile
-  static constexpr int kQ = 0;             // two query tiles
+  static constexpr int kKeyBytes = P8 ? 128 : 64;  // bytes of 128 keys of P or V^T
+  static constexpr int kTileV = D * kKeyBytes;     // D channels x 128 keys
+  static constexpr int kTileP = 128 * kKeyBytes;   // 128 query rows x 128 keys
+  static constexpr int kSFAtoms = D / 64;          // NVFP4 scale atoms per 128-row tile
+  static constexpr int kQ = 0;                     // two query tiles
   static constexpr int kK = kQ + 2 * kTileQK;
   static constexpr int kV = kK + kStages * kTileQK;
-  static constexpr int kP = kV + kStages * kTileV;  // two P tiles of 128 x 64 bytes
-  static constexpr int kOnes = kP + 2 * 8192;       // 16 rows x 64 bytes of E2M1 ones
-  static constexpr int kSFQ = kOnes + 1024;
+  static constexpr int kP = kV + kStages * kTileV;  // two P tiles
+  static constexpr int kOnes = kP + 2 * kTileP;     // 16 rows of ones (E2M1 or E4M3)
+  static constexpr int kSFQ = kOnes + 16 * kKeyBytes;
   static constexpr int kSFK = kSFQ + 2 * kSFAtoms * 512;
   static constexpr int kSFV = kSFK + kStages * kSFAtoms * 512;
   static constexpr int kSFP = kSFV + kStages * 512;
@@ -121,11 +126,11 @@ __device__ __forceinline__ float exp2_int(int e) {  // 2^e, e >= -149
   return 0.0f;
 }
 
-template <int D, bool DUMP, bool CAUSAL>
+template <int D, bool DUMP, bool CAUSAL, bool P8>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_directp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using L = Layout<D>;
+  using L = Layout<D, P8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
@@ -170,8 +175,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // constant operands of the denominator MMA: E2M1 ones (0x22 = two 1.0 codes)
   // and unit E8M0 scales (0x7F = 2^0)
-  for (int i = threadIdx.x; i < 1024 / 16; i += kThreads)
-    reinterpret_cast<uint4*>(smem + L::kOnes)[i] = make_uint4(0x22222222u, 0x22222222u, 0x22222222u, 0x22222222u);
+  // (E4M3 ones are 0x38 bytes in the FP8 P/V variant)
+  constexpr uint32_t kOnes4 = P8 ? 0x38383838u : 0x22222222u;
+  for (int i = threadIdx.x; i < 16 * L::kKeyBytes / 16; i += kThreads)
+    reinterpret_cast<uint4*>(smem + L::kOnes)[i] = make_uint4(kOnes4, kOnes4, kOnes4, kOnes4);
   for (int i = threadIdx.x; i < 512 / 16; i += kThreads)
     reinterpret_cast<uint4*>(smem + L::kSFOnes)[i] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
   fence_proxy_async_smem();
@@ -217,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (leader) {
         mbar_arrive_expect_tx(bar_kv_full + s, L::kTileQK + L::kTileV + kSfBytes + 512);
         tma_load_3d(smem + L::kK + s * L::kTileQK, &tm_k, bar_kv_full + s, 0, j * 128, bh);
-        tma_load_2d(smem + L::kV + s * L::kTileV, &tm_v, bar_kv_full + s, j * 64, bh * D);
+        tma_load_2d(smem + L::kV + s * L::kTileV, &tm_v, bar_kv_full + s, j * L::kKeyBytes, bh * D);
         bulk_load(smem + L::kSFK + s * kSfBytes, p.k_sf + (static_cast<size_t>(bh) * p.ntiles + j) * kSfBytes,
                   kSfBytes, bar_kv_full + s);
         bulk_load(smem + L::kSFV + s * 512, p.v_sf + (static_cast<size_t>(bh) * p.ntiles + j) * 512, 512,
@@ -246,14 +253,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc_pv1 = idesc_fp4_block_scaled(128, D, 1, 2, 2);
     constexpr uint32_t idesc_l0 = idesc_fp4_block_scaled(128, kLN, 1, 0, 0);
     constexpr uint32_t idesc_l1 = idesc_fp4_block_scaled(128, kLN, 1, 2, 2);
+    // P, V^T and the ones tile: K-major rows of 64 bytes (E2M1, 64-byte
+    // swizzle) or 128 bytes (E4M3, 128-byte swizzle); 8-row groups apart by SBO.
+    constexpr uint32_t kSwizzleKV = P8 ? 2u : 4u;
+    constexpr uint32_t kSboKV = 8 * L::kKeyBytes;
     // Descriptors are built once; the start-address field is linear in the
     // shared-memory address (16-byte units), so tiles are reached by adding
     // their offset.
     const uint64_t qdesc = smem_desc(smem_u32(smem + L::kQ + t * L::kTileQK), 16, kSbo, kSwizzleQK);
     const uint64_t kdesc0 = smem_desc(smem_u32(smem + L::kK), 16, kSbo, kSwizzleQK);
-    const uint64_t vdesc0 = smem_desc(smem_u32(smem + L::kV), 16, 512, 4);
-    const uint64_t pdesc = smem_desc(smem_u32(smem + L::kP + t * 8192), 16, 512, 4);
-    const uint64_t ones_desc = smem_desc(smem_u32(smem + L::kOnes), 16, 512, 4);
+    const uint64_t vdesc0 = smem_desc(smem_u32(smem + L::kV), 16, kSboKV, kSwizzleKV);
+    const uint64_t pdesc = smem_desc(smem_u32(smem + L::kP + t * L::kTileP), 16, kSboKV, kSwizzleKV);
+    const uint64_t ones_desc = smem_desc(smem_u32(smem + L::kOnes), 16, kSboKV, kSwizzleKV);
     constexpr uint64_t kQKStep = L::kTileQK >> 4, kVStep = L::kTileV >> 4;
     const uint32_t t_s = tmem + kColS;
     const uint32_t t_o = tmem + kColO + t * D;
@@ -301,10 +312,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t vd = vdesc0 + s * kVStep;
       tc_cp_sf_atom_warp(t_sfp, sfp_src);
       tc_cp_sf_atom_warp(sfv, sfv_src + s * 512);
-      mma_mxf4_warp(t_o, pdesc, vd, idesc_pv0, t_sfp, sfv, j > 0);
-      mma_mxf4_warp(t_o, pdesc + 2, vd + 2, idesc_pv1, t_sfp, sfv, true);
-      mma_mxf4_warp(t_l, pdesc, ones_desc, idesc_l0, t_sfp, t_sf1, false);
-      mma_mxf4_warp(t_l, pdesc + 2, ones_desc + 2, idesc_l1, t_sfp, t_sf1, true);
+      if constexpr (P8) {
+        // E4M3 operands: four K = 32 products per 128 keys, each with the
+        // scale byte k of its 32-key block (one scale per row and block)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_mxf8_warp(t_o, pdesc + 2 * k, vd + 2 * k, idesc_mxf8_block_scaled(128, D, k, k), t_sfp, sfv,
+                        j > 0 || k > 0);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_mxf8_warp(t_l, pdesc + 2 * k, ones_desc + 2 * k, idesc_mxf8_block_scaled(128, kLN, k, k), t_sfp,
+                        t_sf1, k > 0);
+      } else {
+        mma_mxf4_warp(t_o, pdesc, vd, idesc_pv0, t_sfp, sfv, j > 0);
+        mma_mxf4_warp(t_o, pdesc + 2, vd + 2, idesc_pv1, t_sfp, sfv, true);
+        mma_mxf4_warp(t_l, pdesc, ones_desc, idesc_l0, t_sfp, t_sf1, false);
+        mma_mxf4_warp(t_l, pdesc + 2, ones_desc + 2, idesc_l1, t_sfp, t_sf1, true);
+      }
       tc_commit_warp(o_full);
       tc_commit_warp(bar_kv_empty + s);
       // a stage that tile 0 does not consume still needs both releases
@@ -355,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* s_free = bar_s_free + t;
     uint64_t* p_full = bar_p_full + t;
     uint64_t* o_full = bar_o_full + t;
-    uint8_t* sP = smem + L::kP + t * 8192;
+    uint8_t* sP = smem + L::kP + t * L::kTileP;
     uint8_t* sSFP = smem + L::kSFP + t * 512;
     const float c = static_cast<float>(((static_cast<double>(p.softmax_scale) * kLog2E) *
                                         static_cast<double>(*p.g_q)) * static_cast<double>(*p.g_k));
@@ -410,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int b = 0; b < 4; ++b) {
         xb[b] = __fmul_rn(c, bm[b]);
         xmax = fmaxf(xmax, xb[b]);
-        kb[b] = (xb[b] == -INFINITY) ? 0 : static_cast<int>(ceilf(__fsub_rn(xb[b], kLog2Six)));
+        kb[b] = (xb[b] == -INFINITY) ? 0 : static_cast<int>(ceilf(__fsub_rn(xb[b], P8 ? kLog2_448 : kLog2Six)));
       }
       const int m_tile = static_cast<int>(ceilf(xmax));
       const int m_old = m_ref;
@@ -421,8 +445,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_ref = m_tile;
         rescale = true;
       }
-      // Direct-P: codes of 2^(X - K_b) = 2^(c*s - K_b), eight per word
-      uint32_t w[16];
+      // Direct-P: codes of 2^(X - K_b) = 2^(c*s - K_b), eight E2M1 or four
+      // E4M3 codes per word
+      constexpr int kWords = L::kKeyBytes / 4;
+      uint32_t w[kWords];
       uint32_t sfword = 0;
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
@@ -435,7 +461,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 8; i += 2) ffma2(x[i], x[i + 1], c, c, sv[i], sv[i + 1], nk, nk);
 #pragma unroll
           for (int i = 0; i < 8; ++i) x[i] = ex2_approx(x[i]);
-          w[4 * b + q] = cvt_e2m1x8(x[0], x[1], x[2], x[3], x[4], x[5], x[6], x[7]);
+          if constexpr (P8) {
+            w[8 * b + 2 * q] = cvt_e4m3x4(x[0], x[1], x[2], x[3]);
+            w[8 * b + 2 * q + 1] = cvt_e4m3x4(x[4], x[5], x[6], x[7]);
+          } else {
+            w[4 * b + q] = cvt_e2m1x8(x[0], x[1], x[2], x[3], x[4], x[5], x[6], x[7]);
+          }
         }
         int e = kb[b] - m_ref;
         e = e < -127 ? -127 : e;
@@ -474,18 +505,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
       }
-      uint8_t* prow = sP + row * 64;
+      uint8_t* prow = sP + row * L::kKeyBytes;
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int chunk = b ^ ((row >> 1) & 3);  // 64-byte swizzle of the K-major P tile
-        *reinterpret_cast<uint4*>(prow + chunk * 16) = make_uint4(w[4 * b], w[4 * b + 1], w[4 * b + 2], w[4 * b + 3]);
+      for (int u = 0; u < kWords / 4; ++u) {
+        // 64-byte (E2M1) or 128-byte (E4M3) swizzle of the K-major P tile
+        const int chunk = P8 ? (u ^ (row & 7)) : (u ^ ((row >> 1) & 3));
+        *reinterpret_cast<uint4*>(prow + chunk * 16) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
       }
       *reinterpret_cast<uint32_t*>(sSFP + (row & 31) * 16 + (row >> 5) * 4) = sfword;
       if (dump_row) {
         const size_t rr = static_cast<size_t>(qrow - p.dump_row0);
-        uint4* dst = reinterpret_cast<uint4*>(p.dump_codes + rr * (p.ntiles * 64) + j * 64);
+        uint4* dst = reinterpret_cast<uint4*>(p.dump_codes + rr * (p.ntiles * L::kKeyBytes) + j * L::kKeyBytes);
 #pragma unroll
-        for (int b = 0; b < 4; ++b) dst[b] = make_uint4(w[4 * b], w[4 * b + 1], w[4 * b + 2], w[4 * b + 3]);
+        for (int u = 0; u < kWords / 4; ++u) dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
 #pragma unroll
         for (int b = 0; b < 4; ++b) p.dump_kshift[rr * (p.ntiles * 4) + j * 4 + b] = kb[b];
       }
@@ -569,11 +601,13 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool DUMP, bool CAUSAL = false>
+// v: the V payload and scale atoms -- MXFP4 (E2M1) or, with P8, MXFP8 (E4M3)
+// V^T with one byte per key; both use the same atom layout.
+template <int D, bool DUMP, bool CAUSAL = false, bool P8 = false>
 int launch(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k, const fp4attn_mxfp4_t* v, void* o, float* lse,
            int B, int H, int N, float softmax_scale, int dump_bh, int row0, int nrows, uint8_t* codes,
            int32_t* kshift, float* o_f32, cudaStream_t stream, DeviceStatus* status_word = nullptr) {
-  using L = Layout<D>;
+  using L = Layout<D, P8>;
   DeviceStatus* status = status_word ? status_word : device_status_ptr();
   if (!status) return FP4ATTN_ERR_CUDA;
   const int ntiles = n_row_tiles(N);
@@ -584,12 +618,13 @@ int launch(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k, const fp4attn_mxf
                                  static_cast<cuuint64_t>(BH)};
   const cuuint64_t qk_strides[2] = {static_cast<cuuint64_t>(D / 2), static_cast<cuuint64_t>(N) * (D / 2)};
   const cuuint32_t qk_box[3] = {static_cast<cuuint32_t>(D / 2), 128, 1};
-  const cuuint64_t v_dims[2] = {static_cast<cuuint64_t>(ntiles) * 64, static_cast<cuuint64_t>(BH) * D};
-  const cuuint64_t v_strides[1] = {static_cast<cuuint64_t>(ntiles) * 64};
-  const cuuint32_t v_box[2] = {64, static_cast<cuuint32_t>(D)};
+  const cuuint64_t v_dims[2] = {static_cast<cuuint64_t>(ntiles) * L::kKeyBytes, static_cast<cuuint64_t>(BH) * D};
+  const cuuint64_t v_strides[1] = {static_cast<cuuint64_t>(ntiles) * L::kKeyBytes};
+  const cuuint32_t v_box[2] = {static_cast<cuuint32_t>(L::kKeyBytes), static_cast<cuuint32_t>(D)};
+  const CUtensorMapSwizzle swz_v = P8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   if (!make_map(&tq, q->payload, 3, qk_dims, qk_strides, qk_box, swz_qk) ||
       !make_map(&tk, k->payload, 3, qk_dims, qk_strides, qk_box, swz_qk) ||
-      !make_map(&tv, v->payload_t, 2, v_dims, v_strides, v_box, CU_TENSOR_MAP_SWIZZLE_64B))
+      !make_map(&tv, v->payload_t, 2, v_dims, v_strides, v_box, swz_v))
     return FP4ATTN_ERR_CUDA;
   FwdParams prm{};
   prm.q_sf = q->sf;
@@ -609,7 +644,7 @@ int launch(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k, const fp4attn_mxf
   prm.dump_codes = codes;
   prm.dump_kshift = kshift;
   prm.dump_o = o_f32;
-  auto kern = fwd_directp_kernel<D, DUMP, CAUSAL>;
+  auto kern = fwd_directp_kernel<D, DUMP, CAUSAL, P8>;
   static std::once_flag attr_once[64];
   int dev = 0;
   cudaGetDevice(&dev);
@@ -719,6 +754,55 @@ extern "C" int fp4attn_fwd_directp_causal_save(const void* q, const void* k, con
   if (r == FP4ATTN_OK) r = fp4attn_quant_v_mxfp4(v, v_quant->payload_t, v_quant->sf, B, H, N, D, stream);
   if (r == FP4ATTN_OK) r = fp4attn_fwd_directp_causal(&qn, &kn, &vm, o, lse, B, H, N, D, softmax_scale, stream);
   return r;
+}
+
+extern "C" int fp4attn_fwd_directp_fp8pv(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k,
+                                         const fp4attn_mxfp8_t* v, void* o, float* lse, int B, int H, int N, int D,
+                                         float softmax_scale, int causal, void* stream) {
+  if (!v) return FP4ATTN_ERR_INVALID_ARG;
+  const fp4attn_mxfp4_t vv{v->payload_t, v->sf};  // same two pointers; one byte per key
+  const int st = check_fwd(q, k, &vv, o, lse, B, H, N, D, softmax_scale);
+  if (st != FP4ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (D == 128)
+    return causal ? launch<128, false, true, true>(q, k, &vv, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr,
+                                                   nullptr, nullptr, s)
+                  : launch<128, false, false, true>(q, k, &vv, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr,
+                                                    nullptr, nullptr, s);
+  return causal ? launch<64, false, true, true>(q, k, &vv, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr,
+                                                nullptr, nullptr, s)
+                : launch<64, false, false, true>(q, k, &vv, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr,
+                                                 nullptr, nullptr, s);
+}
+
+extern "C" int fp4attn_debug_dump_p_fp8pv(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k,
+                                          const fp4attn_mxfp8_t* v, void* o, float* lse, int B, int H, int N, int D,
+                                          float softmax_scale, int causal, int b, int h, int row0, int nrows,
+                                          uint8_t* codes, int32_t* kshift, float* o_f32, void* stream) {
+  if (!v) return FP4ATTN_ERR_INVALID_ARG;
+  const fp4attn_mxfp4_t vv{v->payload_t, v->sf};
+  const int st = check_fwd(q, k, &vv, o, lse, B, H, N, D, softmax_scale);
+  if (st != FP4ATTN_OK) return st;
+  if (b < 0 || b >= B || h < 0 || h >= H || row0 < 0 || nrows <= 0 || row0 + nrows > N || !codes || !kshift ||
+      !o_f32 || !aligned16(codes) || !aligned16(kshift) || !aligned16(o_f32))
+    return FP4ATTN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // key tiles past a row's diagonal (causal) are never visited: their codes
+  // and shifts read as zero
+  const size_t npad = static_cast<size_t>(n_row_tiles(N)) * 128;
+  if (cudaMemsetAsync(codes, 0, static_cast<size_t>(nrows) * npad, s) != cudaSuccess ||
+      cudaMemsetAsync(kshift, 0, static_cast<size_t>(nrows) * (npad / 32) * sizeof(int32_t), s) != cudaSuccess)
+    return FP4ATTN_ERR_CUDA;
+  const int bh = b * H + h;
+  if (D == 128)
+    return causal ? launch<128, true, true, true>(q, k, &vv, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes,
+                                                  kshift, o_f32, s)
+                  : launch<128, true, false, true>(q, k, &vv, o, lse, B, H, N, softmax_scale, bh, row0, nrows,
+                                                   codes, kshift, o_f32, s);
+  return causal ? launch<64, true, true, true>(q, k, &vv, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes,
+                                               kshift, o_f32, s)
+                : launch<64, true, false, true>(q, k, &vv, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes,
+                                                kshift, o_f32, s);
 }
 
 // ------------------------------------------------------------------ allocation-free variant

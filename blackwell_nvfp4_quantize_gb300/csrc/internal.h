@@ -37,6 +37,9 @@ inline size_t nvfp4_sf_bytes(int B, int H, int N, int D) {
 inline size_t mxfp4_payload_bytes(int B, int H, int N, int D) {
   return static_cast<size_t>(B) * H * D * (n_row_tiles(N) * 64);
 }
+inline size_t mxfp8_payload_bytes(int B, int H, int N, int D) {
+  return static_cast<size_t>(B) * H * D * (n_row_tiles(N) * 128);
+}
 inline size_t mxfp4_sf_bytes(int B, int H, int N, int /*D*/) {
   return static_cast<size_t>(B) * H * n_row_tiles(N) * 512;
 }

@@ -180,6 +180,15 @@ __host__ __device__ constexpr uint32_t idesc_fp4_block_scaled(uint32_t M, uint32
          ((M >> 4) & 0x1Fu) << 24 | (a_sf_id & 3u) << 29;
 }
 
+// Instruction descriptor of kind::mxf8f6f4 with E4M3 A and B (format 0),
+// K-major, fp32 accumulate, UE8M0 scales (one per 32-element block), and the
+// byte of the 32-bit scale column each operand's scale is taken from.
+__host__ __device__ constexpr uint32_t idesc_mxf8_block_scaled(uint32_t M, uint32_t N, uint32_t a_sf_id,
+                                                               uint32_t b_sf_id) {
+  return (b_sf_id & 3u) << 4 | ((N >> 3) & 0x3Fu) << 17 | (1u << 23) | ((M >> 4) & 0x1Fu) << 24 |
+         (a_sf_id & 3u) << 29;
+}
+
 // D[tmem] (+)= A[smem] x B[smem]^T with NVFP4 scales (16-element blocks, UE4M3).
 __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t sfa_tmem, uint32_t sfb_tmem, bool accumulate) {
@@ -226,6 +235,15 @@ __device__ __forceinline__ void mma_mxf4_warp(uint32_t d_tmem, uint64_t adesc, u
   asm volatile(
       "{\n.reg .pred p, e;\nsetp.ne.b32 p, %6, 0;\nelect.sync _|e, 0xffffffff;\n"
       "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n}\n"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate ? 1 : 0)
+      : "memory");
+}
+// E4M3 x E4M3 with one UE8M0 scale per 32-element block (K = 32 per MMA).
+__device__ __forceinline__ void mma_mxf8_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t sfa_tmem, uint32_t sfb_tmem, bool accumulate) {
+  asm volatile(
+      "{\n.reg .pred p, e;\nsetp.ne.b32 p, %6, 0;\nelect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n"
       ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate ? 1 : 0)
       : "memory");
 }
@@ -338,6 +356,18 @@ __device__ __forceinline__ uint32_t cvt_e4m3(float x) {
   uint16_t r;  // both halves receive x, so the byte order of the pair does not matter
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(r) : "f"(x));
   return r & 0xFFu;
+}
+// Four fp32 values -> four E4M3 codes (round to nearest even, saturating),
+// x0 in the low byte.
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float x0, float x1, float x2, float x3) {
+  uint32_t r;
+  asm("{\n.reg .b16 lo, hi;\n"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n"
+      "mov.b32 %0, {lo, hi};\n}\n"
+      : "=r"(r)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
+  return r;
 }
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

@@ -7,6 +7,9 @@
 //  nvfp4_finalize     : g = amax / 2688 (1 for an all-zero tensor)
 //  mxfp4_v_kernel     : 32-key blocks per channel, E8M0 scale, codes written
 //                       key-inner (V transposed) through shared memory
+//  mxfp8_v_kernel     : the same for E4M3 codes (the FP8 P/V variant:
+//                       training keeps FP8 probabilities and values), one
+//                       byte per key
 //
 // All three data kernels are HBM-bound streaming passes: 16-byte vector loads,
 // grid sized in multiples of the SM count, warp-shuffle reductions, and
@@ -176,6 +179,60 @@ __global__ void __launch_bounds__(256) mxfp4_v_kernel(const uint4* __restrict__ 
         reinterpret_cast<const uint4*>(atom)[threadIdx.x];
 }
 
+// MXFP8 V: the same staging and atoms as mxfp4_v_kernel; the scale is the
+// smallest 2^e with amax <= 448 * 2^e and each key keeps one E4M3 byte.
+template <int D>
+__global__ void __launch_bounds__(256) mxfp8_v_kernel(const uint4* __restrict__ v, uint8_t* __restrict__ payload_t,
+                                                      uint8_t* __restrict__ sf, int N) {
+  __shared__ __align__(16) uint16_t tile[128 * D];
+  __shared__ __align__(16) uint32_t atom[128];
+  const int kt = blockIdx.x;
+  const long long bh = blockIdx.y;
+  const int ntiles = gridDim.x;
+  const int npad = ntiles * 128;  // bytes per V^T row
+  constexpr int VPR = D / 8;
+  for (int i = threadIdx.x; i < 128 * VPR; i += 256) {
+    const int r = i / VPR, cv = i % VPR;
+    const int n = kt * 128 + r;
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (n < N) val = __ldcs(v + ((bh * N + n) * VPR + cv));
+    *reinterpret_cast<uint4*>(&tile[r * D + cv * 8]) = val;
+  }
+  if (threadIdx.x < 128) atom[threadIdx.x] = 0u;
+  __syncthreads();
+  for (int pidx = threadIdx.x; pidx < 4 * D; pidx += 256) {
+    const int d = pidx % D, kb = pidx / D;
+    uint32_t h[32];
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      h[i] = tile[(kb * 32 + i) * D + d];
+      m = max(m, h[i] & 0x7FFFu);
+    }
+    // e = smallest integer >= -127 with amax <= 448 * 2^e (448 = 1.75 * 2^8),
+    // from the bits of amax
+    const uint32_t ebits = m >> 7, frac = m & 0x7Fu;
+    int e = -127;
+    if (ebits != 0) e = max(-127, static_cast<int>(ebits) - 127 - (frac <= 0x60u ? 8 : 7));
+    const float inv_scale = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, e <= 121
+    uint32_t wd[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      wd[i] = cvt_e4m3x4(__fmul_rn(__uint_as_float(h[4 * i] << 16), inv_scale),
+                         __fmul_rn(__uint_as_float(h[4 * i + 1] << 16), inv_scale),
+                         __fmul_rn(__uint_as_float(h[4 * i + 2] << 16), inv_scale),
+                         __fmul_rn(__uint_as_float(h[4 * i + 3] << 16), inv_scale));
+    uint4* dst = reinterpret_cast<uint4*>(payload_t + (bh * D + d) * npad + kt * 128 + kb * 32);
+    __stcs(dst, make_uint4(wd[0], wd[1], wd[2], wd[3]));
+    __stcs(dst + 1, make_uint4(wd[4], wd[5], wd[6], wd[7]));
+    reinterpret_cast<uint8_t*>(atom)[(d & 31) * 16 + (d >> 5) * 4 + kb] = static_cast<uint8_t>(e + 127);
+  }
+  __syncthreads();
+  if (threadIdx.x < 32)
+    reinterpret_cast<uint4*>(sf + (bh * ntiles + kt) * 512)[threadIdx.x] =
+        reinterpret_cast<const uint4*>(atom)[threadIdx.x];
+}
+
 int grid_for(long long work_items, int threads) {
   const long long want = (work_items + threads - 1) / threads;
   const long long cap = static_cast<long long>(sm_count()) * 8;  // 8 x 256 threads per SM
@@ -220,5 +277,20 @@ extern "C" int fp4attn_quant_v_mxfp4(const void* v, uint8_t* payload_t, uint8_t*
     mxfp4_v_kernel<128><<<grid, 256, 0, s>>>(static_cast<const uint4*>(v), payload_t, sf, N);
   else
     mxfp4_v_kernel<64><<<grid, 256, 0, s>>>(static_cast<const uint4*>(v), payload_t, sf, N);
+  return cuda_status(cudaGetLastError());
+}
+
+extern "C" int fp4attn_quant_v_mxfp8(const void* v, uint8_t* payload_t, uint8_t* sf, int B, int H, int N, int D,
+                                     void* stream) {
+  int st = check_shape(B, H, N, D);
+  if (st != FP4ATTN_OK) return st;
+  if (!v || !payload_t || !sf) return FP4ATTN_ERR_INVALID_ARG;
+  if (!aligned16(v) || !aligned16(payload_t) || !aligned16(sf)) return FP4ATTN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  dim3 grid(n_row_tiles(N), B * H);
+  if (D == 128)
+    mxfp8_v_kernel<128><<<grid, 256, 0, s>>>(static_cast<const uint4*>(v), payload_t, sf, N);
+  else
+    mxfp8_v_kernel<64><<<grid, 256, 0, s>>>(static_cast<const uint4*>(v), payload_t, sf, N);
   return cuda_status(cudaGetLastError());
 }

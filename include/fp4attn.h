@@ -47,6 +47,13 @@
  *     V scales:   atom [b*H + h][n / 128], rows = channels d (D <= 128,
  *                 rows >= D are 0), blocks = 32-key groups of that tile
  *   LSE:                  fp32 [B, H, N]
+ *   FP8 P/V variant (MXFP8 V, E4M3 probability codes; "What the paper
+ *   found": training keeps FP8 probabilities and values):
+ *     V payload: [B, H, D, Npad] bytes, one E4M3 code per key (keys >= N: 0);
+ *     V scales:  exactly the MXFP4 V atoms; e is the smallest integer >= -127
+ *                with amax <= 448 * 2^e, code = E4M3(v * 2^-e);
+ *     P codes:   E4M3(2^(X - K_b)) with K_b = ceil(X_b - log2 448); the rest
+ *                of the Direct-P definition is unchanged.
  *
  * Supported shapes: D in {64, 128}; B, H, N >= 1; B*H*N < 2^31.  The
  * quantizers accept any N; fp4attn_fwd_directp accepts any N >= 1 (a partial
@@ -84,6 +91,12 @@ typedef struct {
     const uint8_t *sf;        /* scale atoms, fp4attn_mxfp4_v_bytes(...).sf bytes */
 } fp4attn_mxfp4_t;
 
+/* Quantized MXFP8 V as written by fp4attn_quant_v_mxfp8. */
+typedef struct {
+    const uint8_t *payload_t; /* [B,H,D,Npad] */
+    const uint8_t *sf;        /* scale atoms, fp4attn_mxfp8_v_bytes(...).sf bytes */
+} fp4attn_mxfp8_t;
+
 /* Writable buffers of a quantized NVFP4 tensor (outputs of a call). */
 typedef struct {
     uint8_t *payload; /* [B,H,N,D/2] */
@@ -107,6 +120,9 @@ int fp4attn_nvfp4_bytes(int B, int H, int N, int D, size_t *payload_bytes, size_
 /* Sizes in bytes of the MXFP4 V buffers for a [B,H,N,D] tensor. */
 int fp4attn_mxfp4_v_bytes(int B, int H, int N, int D, size_t *payload_bytes, size_t *sf_bytes);
 
+/* Sizes in bytes of the MXFP8 V buffers for a [B,H,N,D] tensor. */
+int fp4attn_mxfp8_v_bytes(int B, int H, int N, int D, size_t *payload_bytes, size_t *sf_bytes);
+
 /* NVFP4-quantize Q or K ("What the paper found": NVFP4 for Q and K).
  * x: bf16 [B,H,N,D] (device, read only).  Writes payload, sf (every byte of
  * the padded atoms) and *g (device, 4 bytes; used as the amax accumulator
@@ -120,6 +136,13 @@ int fp4attn_quant_qk_nvfp4(const void *x, uint8_t *payload, uint8_t *sf, float *
  * v: bf16 [B,H,N,D].  Writes payload_t and sf (all bytes, padding included).
  * One kernel; inputs must be finite. */
 int fp4attn_quant_v_mxfp4(const void *v, uint8_t *payload_t, uint8_t *sf,
+                          int B, int H, int N, int D, void *stream);
+
+/* MXFP8-quantize V along the key axis, written key-inner (the FP8 P/V
+ * variant: "What the paper found", training keeps FP8 probabilities and
+ * values).  v: bf16 [B,H,N,D].  Writes payload_t and sf (all bytes, padding
+ * included).  One kernel; inputs must be finite. */
+int fp4attn_quant_v_mxfp8(const void *v, uint8_t *payload_t, uint8_t *sf,
                           int B, int H, int N, int D, void *stream);
 
 /* Noncausal Direct-P forward (abstract: "Direct-P for noncausal inference";
@@ -144,6 +167,18 @@ int fp4attn_fwd_directp(const fp4attn_nvfp4_t *q, const fp4attn_nvfp4_t *k, cons
 int fp4attn_fwd_directp_causal(const fp4attn_nvfp4_t *q, const fp4attn_nvfp4_t *k, const fp4attn_mxfp4_t *v,
                                void *o, float *lse, int B, int H, int N, int D, float softmax_scale,
                                void *stream);
+
+/* Direct-P forward with FP8 P/V operands ("What the paper found": FP8
+ * probabilities and values are kept for training; abstract: matched
+ * training retains FP8 probabilities and values).  Q and K stay NVFP4; V is
+ * MXFP8 (fp4attn_quant_v_mxfp8); the probability codes are E4M3 with the
+ * block shift K_b = ceil(X_b - log2 448) and the PV product runs on E4M3
+ * operands with UE8M0 block scales.  causal != 0: query row i attends to keys
+ * 0 .. i (as fp4attn_fwd_directp_causal), otherwise to all keys.  Other
+ * arguments, layouts and errors as fp4attn_fwd_directp.  One kernel launch. */
+int fp4attn_fwd_directp_fp8pv(const fp4attn_nvfp4_t *q, const fp4attn_nvfp4_t *k, const fp4attn_mxfp8_t *v,
+                              void *o, float *lse, int B, int H, int N, int D, float softmax_scale, int causal,
+                              void *stream);
 
 /* The causal training forward in one call: NVFP4-quantizes q and k (bf16
  * [B,H,N,D], device) into the caller's q_saved and k_saved buffers,
@@ -205,6 +240,14 @@ int fp4attn_debug_dump_p_causal(const fp4attn_nvfp4_t *q, const fp4attn_nvfp4_t 
                                 void *o, float *lse, int B, int H, int N, int D, float softmax_scale,
                                 int b, int h, int row0, int nrows, uint8_t *codes, int32_t *kshift,
                                 float *o_f32, void *stream);
+
+/* fp4attn_debug_dump_p for the FP8 P/V forward: codes are E4M3 bytes,
+ * [nrows, Npad] (one byte per key); kshift and o_f32 as there.  Clears codes
+ * and kshift on stream first. */
+int fp4attn_debug_dump_p_fp8pv(const fp4attn_nvfp4_t *q, const fp4attn_nvfp4_t *k, const fp4attn_mxfp8_t *v,
+                               void *o, float *lse, int B, int H, int N, int D, float softmax_scale, int causal,
+                               int b, int h, int row0, int nrows, uint8_t *codes, int32_t *kshift,
+                               float *o_f32, void *stream);
 
 /* Test support (no counterpart in the method): for format 0 (E2M1) or 1
  * (E4M3), converts every fp32 bit pattern u in [lo, hi] with the hardware

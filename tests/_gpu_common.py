@@ -52,23 +52,29 @@ CODE_AGREE = 0.999
 BF16_REL = 2.0 ** -8
 
 
-def quantize(q, k, v):
+def quantize(q, k, v, fp8pv=False):
     import blackwell_nvfp4_quantize_gb300 as fa
 
-    return fa.quant_qk_nvfp4(q.cuda()), fa.quant_qk_nvfp4(k.cuda()), fa.quant_v_mxfp4(v.cuda())
+    vq = fa.quant_v_mxfp8(v.cuda()) if fp8pv else fa.quant_v_mxfp4(v.cuda())
+    return fa.quant_qk_nvfp4(q.cuda()), fa.quant_qk_nvfp4(k.cuda()), vq
 
 
-def run_and_check(q, k, v, scale, dump_slices, sample, label, causal=False):
-    """Runs the forward (causal: query i sees keys 0..i) and compares it with
-    the oracle.  dump_slices: list of (b, h, row0, nrows) compared in full
-    (codes, block shifts, fp32 O before its bf16 store, LSE); sample: flat row
-    ids whose stored bf16 O and LSE are compared."""
+def run_and_check(q, k, v, scale, dump_slices, sample, label, causal=False, fp8pv=False):
+    """Runs the forward (causal: query i sees keys 0..i; fp8pv: E4M3
+    probability codes and MXFP8 V) and compares it with the oracle.
+    dump_slices: list of (b, h, row0, nrows) compared in full (codes, block
+    shifts, fp32 O before its bf16 store, LSE); sample: flat row ids whose
+    stored bf16 O and LSE are compared."""
     import blackwell_nvfp4_quantize_gb300 as fa
 
     B, H, N, D = q.shape
-    qq, kq, vq = quantize(q, k, v)
-    fwd = fa.fwd_directp_causal if causal else fa.fwd_directp
-    o, lse = fwd(qq, kq, vq, scale)
+    qq, kq, vq = quantize(q, k, v, fp8pv)
+    pv_fmt = oracle.PV_MXFP8 if fp8pv else oracle.PV_MXFP4
+    if fp8pv:
+        o, lse = fa.fwd_directp_fp8pv(qq, kq, vq, scale, causal=causal)
+    else:
+        fwd = fa.fwd_directp_causal if causal else fa.fwd_directp
+        o, lse = fwd(qq, kq, vq, scale)
     torch.cuda.synchronize()
     assert fa.device_status() == fa.FP4ATTN_OK
     qn, kn, vn = nv_to_np(qq), nv_to_np(kq), mx_to_np(vq)
@@ -76,7 +82,7 @@ def run_and_check(q, k, v, scale, dump_slices, sample, label, causal=False):
     lse_np = lse.cpu().numpy().reshape(-1)
     assert np.all(np.isfinite(o_np)) and np.all(np.isfinite(lse_np))
     # stored bf16 O / LSE on sampled rows: 2e-2 plus the bf16 rounding of the output
-    ref = oracle.directp_rows(qn, kn, vn, (B, H, N, D), scale, sample, causal=causal)
+    ref = oracle.directp_rows(qn, kn, vn, (B, H, N, D), scale, sample, causal=causal, pv_fmt=pv_fmt)
     err_o16 = float(np.max(np.abs(o_np[sample] - ref["o"]) - BF16_REL * np.abs(ref["o"])))
     err_l = float(np.max(np.abs(lse_np[sample] - ref["lse"])))
     # codes, block shifts and fp32 O through the dump entry point (same kernel and launch shape)
@@ -89,10 +95,11 @@ def run_and_check(q, k, v, scale, dump_slices, sample, label, causal=False):
         assert torch.equal(o2, o) and torch.equal(lse2, lse)
         assert torch.equal(o32.to(torch.bfloat16), o2.reshape(-1, D)[(b * H + h) * N + row0:][:nrows])
         rows = np.arange(nrows, dtype=np.int64) + (b * H + h) * N + row0
-        r = oracle.directp_rows(qn, kn, vn, (B, H, N, D), scale, rows, want_codes=True, causal=causal)
+        r = oracle.directp_rows(qn, kn, vn, (B, H, N, D), scale, rows, want_codes=True, causal=causal,
+                                pv_fmt=pv_fmt)
         err_o32 = max(err_o32, float(np.max(np.abs(o32.cpu().numpy() - r["o"]))))
         err_l = max(err_l, float(np.max(np.abs(lse_np[rows] - r["lse"]))))
-        gc = unpack_codes(codes.cpu().numpy())
+        gc = codes.cpu().numpy() if fp8pv else unpack_codes(codes.cpu().numpy())
         agree += int(np.sum(gc[:, :N] == r["codes"][:, :N]))
         total += nrows * N
         nblk = (N + 31) // 32

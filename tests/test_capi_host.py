@@ -115,3 +115,22 @@ def test_causal_argument_errors_without_gpu(L):
     assert L.fp4attn_fwd_directp_causal_save(good, good, good, ctypes.byref(q), ctypes.byref(q), ctypes.byref(v),
                                              good, good, 1, 1, 128, 64, ctypes.c_float(0.0), n) == \
         fa.FP4ATTN_ERR_INVALID_ARG
+
+
+def test_fp8pv_argument_errors_without_gpu(L):
+    import blackwell_nvfp4_quantize_gb300 as fa
+
+    n = None
+    q = fa._NVFP4(0x1000, 0x2000, 0x3000)
+    v = fa._MXFP4(0x4000, 0x5000)
+    good = ctypes.c_void_p(0x6000)
+    assert fa.mxfp8_v_bytes(1, 40, 32768, 128) == (40 * 128 * 32768, 40 * 256 * 512)
+    assert fa.mxfp8_v_bytes(2, 3, 77, 64) == (6 * 64 * 128, 6 * 512)
+    assert L.fp4attn_quant_v_mxfp8(n, good, good, 1, 1, 128, 64, n) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert L.fp4attn_quant_v_mxfp8(good, good, good, 1, 1, 128, 96, n) == fa.FP4ATTN_ERR_UNSUPPORTED
+    args = (ctypes.byref(q), ctypes.byref(q), ctypes.byref(v), good, good, 1, 1, 128, 64)
+    assert L.fp4attn_fwd_directp_fp8pv(*args, ctypes.c_float(0.0), 0, n) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert L.fp4attn_fwd_directp_fp8pv(ctypes.byref(q), ctypes.byref(q), None, good, good, 1, 1, 128, 64,
+                                       ctypes.c_float(0.1), 1, n) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert L.fp4attn_debug_dump_p_fp8pv(*args, ctypes.c_float(0.1), 0, 0, 0, 100, 64, good, good, good, n) == \
+        fa.FP4ATTN_ERR_INVALID_ARG  # rows beyond N
