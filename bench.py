@@ -144,6 +144,24 @@ def attn_flops(rows, N, D, causal):
     return 4.0 * D * float(keys)
 
 
+def max_over_ranks(values, dist=None, device=None):
+    """Each timing (ms) maximised over the ranks of the process group (the
+    slowest replica sets the whole job's time); the values as they are for one
+    process."""
+    if dist is None:
+        return [float(x) for x in values]
+    import torch
+
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_tflops(world, flops_per_replica, ms):
+    """Throughput of the whole job: every rank runs one replica of the workload."""
+    return world * flops_per_replica / (ms * 1e-3) / 1e12
+
+
 def cpu_baseline(w, q, k, v, causal=False, fp8pv=False, budget_s=12.0):
     """The oracle as it stands, on host cores, on a bounded row sample of head 0."""
     import numpy as np
@@ -357,14 +375,11 @@ def run_ours(args, w):
     if fa.device_status() != fa.FP4ATTN_OK:
         raise RuntimeError("device-side wait timed out in the end-to-end leg")
 
-    if dist is not None:
-        t = torch.tensor([ms_total, e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total, e2e_ms = float(t[0]), float(t[1])
+    ms_total, e2e_ms = max_over_ranks([ms_total, e2e_ms], dist, dev)
 
     flops = B * H * attn_flops(range(N), N, D, args.causal)
     ms_step = ms_total / args.steps
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops, ms_step)
     fwd_avg = sum(fwd_ms) / len(fwd_ms)
     achieved = flops / (fwd_avg * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
@@ -390,7 +405,7 @@ def run_ours(args, w):
                                      % (peak_src, ratio, "FP4-QK/FP8-PV:BF16" if args.fp8pv else "FP4:BF16")),
                      "kernel": "fwd_directp_kernel<%d, causal=%s, fp8pv=%s>"
                                % (D, str(bool(args.causal)).lower(), str(bool(args.fp8pv)).lower())},
-        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        "e2e": {"value": whole_job_tflops(world, flops, e2e_ms), "unit": UNIT,
                 "pipelining": "upload of step i+1 and download of step i-1 overlap step i's kernels",
                 "h2d_bytes_per_step": 3 * B * H * N * D * 2, "d2h_bytes_per_step": B * H * N * D * 2 + B * H * N * 4},
         "gpu_launches": launches_per_step * args.steps,
