@@ -82,7 +82,8 @@ def lib():
     L.fp4attn_debug_dump_p_fp8pv.argtypes = [ctypes.POINTER(_NVFP4), ctypes.POINTER(_NVFP4),
                                              ctypes.POINTER(_MXFP4), vp, vp, i, i, i, i, f, i, i, i, i, i, vp, vp,
                                              vp, vp]
-    for name in ("fp4attn_mxfp8_v_bytes", "fp4attn_quant_v_mxfp8", "fp4attn_fwd_directp_fp8pv",
+    L.fp4attn_debug_wait_timeout.argtypes = [i, vp]
+    for name in ("fp4attn_debug_wait_timeout", "fp4attn_mxfp8_v_bytes", "fp4attn_quant_v_mxfp8", "fp4attn_fwd_directp_fp8pv",
                  "fp4attn_debug_dump_p_fp8pv", "fp4attn_fwd_directp_causal", "fp4attn_debug_dump_p_causal", "fp4attn_fwd_directp_causal_save",
                  "fp4attn_fwd_directp_noalloc", "fp4attn_debug_cvt_transitions", "fp4attn_nvfp4_bytes", "fp4attn_mxfp4_v_bytes", "fp4attn_quant_qk_nvfp4",
                  "fp4attn_quant_v_mxfp4", "fp4attn_fwd_directp", "fp4attn_debug_dump_p",
@@ -339,6 +340,12 @@ def debug_dump_p(q: NVFP4Tensor, k: NVFP4Tensor, v, b: int, h: int, row0: int, n
 def device_status(stream=None) -> int:
     """fp4attn_device_status: FP4ATTN_OK, or FP4ATTN_ERR_TIMEOUT if a bounded wait gave up."""
     return lib().fp4attn_device_status(ctypes.c_void_p(_stream(stream)))
+
+
+def debug_wait_timeout(limit_us: int, stream=None) -> None:
+    """fp4attn_debug_wait_timeout: a bounded wait that nothing completes gives up after limit_us."""
+    _check(lib().fp4attn_debug_wait_timeout(int(limit_us), ctypes.c_void_p(_stream(stream))),
+           "fp4attn_debug_wait_timeout")
 
 
 def debug_cvt_transitions(fmt: int, lo: int, hi: int, capacity: int = 4096, stream=None):

@@ -39,10 +39,35 @@ __global__ void __launch_bounds__(256) cvt_transitions_kernel(int format, uint32
   }
 }
 
+// The failure path of the bounded waits, exercised without a fault: one warp
+// waits on an mbarrier that nothing ever arrives at, through the same
+// mbar_wait the forward kernel uses but with a short limit, so the wait gives
+// up, records site 90 in the status word, and the kernel returns.
+__global__ void __launch_bounds__(32) wait_timeout_kernel(uint64_t limit_ns, DeviceStatus* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncwarp();
+  mbar_wait(&bar, 0, &abort_flag, status, 90, limit_ns);
+}
+
 }  // namespace
 }  // namespace fp4attn
 
 using namespace fp4attn;
+
+extern "C" int fp4attn_debug_wait_timeout(int limit_us, void* stream) {
+  if (limit_us <= 0 || limit_us > 1000000) return FP4ATTN_ERR_INVALID_ARG;
+  DeviceStatus* status = device_status_ptr();
+  if (!status) return FP4ATTN_ERR_CUDA;
+  wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint64_t>(limit_us) * 1000u,
+                                                                      status);
+  return cuda_status(cudaGetLastError());
+}
 
 extern "C" int fp4attn_debug_cvt_transitions(int format, uint32_t lo, uint32_t hi, uint32_t* pairs, int capacity,
                                              int* count, void* stream) {

@@ -54,16 +54,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait on a phase parity.  Gives up when *abort becomes nonzero (some
-// other role gave up) or after FP4ATTN_WAIT_NS; in the latter case records the
-// failure and raises *abort.
+// other role gave up) or after limit_ns (FP4ATTN_WAIT_NS unless a test asks
+// for less); in the latter case records the failure and raises *abort.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          DeviceStatus* status, unsigned site) {
+                                          DeviceStatus* status, unsigned site,
+                                          uint64_t limit_ns = FP4ATTN_WAIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > FP4ATTN_WAIT_NS) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;
       if (status) {
         if (atomicCAS(&status->timeout, 0u, 1u) == 0u) status->where = site;

@@ -259,6 +259,14 @@ int fp4attn_debug_dump_p_fp8pv(const fp4attn_nvfp4_t *q, const fp4attn_nvfp4_t *
 int fp4attn_debug_cvt_transitions(int format, uint32_t lo, uint32_t hi, uint32_t *pairs, int capacity,
                                   int *count, void *stream);
 
+/* Test support (no counterpart in the method): exercises the failure path of
+ * the bounded device-side waits without any fault.  One warp waits on an
+ * mbarrier that nothing arrives at, through the same bounded wait the forward
+ * uses but limited to limit_us microseconds (1 .. 1000000); the wait gives up,
+ * sets the status word (read it with fp4attn_device_status, which then reports
+ * FP4ATTN_ERR_TIMEOUT once) and the kernel returns normally. */
+int fp4attn_debug_wait_timeout(int limit_us, void *stream);
+
 /* Reads and clears the status word the kernels of this library set when a
  * bounded device-side wait gives up (they then stop early and leave their
  * outputs incomplete).  Synchronises the given stream first.  Returns
