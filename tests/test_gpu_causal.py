@@ -86,3 +86,16 @@ def test_causal_last_row_matches_noncausal():
     assert torch.allclose(oc[:, :, -1].float(), on[:, :, -1].float(), atol=4e-2, rtol=0)
     # the first row sees only key 0 and differs
     assert not torch.equal(lc[:, :, 0], ln[:, :, 0])
+
+
+@pytest.mark.parametrize("causal,fp8pv", [(False, False), (True, False), (False, True), (True, True)])
+def test_long_single_head(causal, fp8pv):
+    # one head with 200000 keys (1563 key tiles, the last one partial): every
+    # index of the kernels and the dump stays in range; rows spread over the
+    # sequence, both ends included
+    N, D = 200000, 128
+    q, k, v = wl.make_custom(1, 1, N, D, seed=41, kind="normal", scale=1.0)
+    rng = np.random.default_rng(41)
+    sample = np.unique(np.concatenate([[0, 1, 127, 128, N - 129, N - 1], rng.choice(N, 10, replace=False)]))
+    run_and_check(q, k, v, 1.0 / math.sqrt(D), [(0, 0, N - 64, 64)], sample.astype(np.int64),
+                  "long head causal=%d fp8pv=%d" % (causal, fp8pv), causal=causal, fp8pv=fp8pv)
