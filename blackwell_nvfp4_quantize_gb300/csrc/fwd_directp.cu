@@ -32,9 +32,14 @@
 // Causal variant (the causal forward of "What the paper found": forward for
 // causal training): key j is seen by query i only when j <= i.  Query tile
 // qt needs the key tiles 0 .. qt, the last one masked along its diagonal, and
-// no others.  CTA c takes the query tiles c and T-1-c (T tiles per head), so
-// every CTA streams T+1 tile-steps of work; the short tile c is tile 0 and
-// drops out after its diagonal, tile T-1-c carries on alone.
+// no others.  Each of the two slots of a CTA (warpgroup + MMA warp) then runs
+// a chain of two query tiles, i and T-1-i (T tiles per head): i+1 key tiles,
+// then T-i, T+1 key steps in all, so both slots take every step together
+// and the score bank keeps alternating between them.  A slot writes out its
+// first tile's O and LSE when it starts on the second.  For odd T the middle
+// tile forms a chain alone; the CTA holding it runs its longer slot alone for
+// the last steps.  With two query tiles per slot the ring holds one K/V tile
+// per slot and stage.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -49,10 +54,9 @@ namespace {
 
 constexpr int kThreads = 352;
 constexpr int kWarpTma = 8, kWarpMma0 = 9;  // warps 9 and 10 issue the MMAs of query tiles 0 and 1
-constexpr int kStages = 3;
-// The MMA warp of a tile issues S = Q K(j+1)^T before its PV product of tile
-// j, so the ring must hold tiles j and j+1 at once.
-static_assert(kStages >= 2, "the K/V ring needs at least two stages");
+// The MMA warp of a slot issues S = Q K(j+1)^T before its PV product of step
+// j, so the ring must hold steps j and j+1 at once: at least two stages.
+constexpr int kRingStages = 3;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;         // 128 columns: fp32 scores of 128 keys
 constexpr uint32_t kColO = 128;       // tile t output at kColO + t * D
@@ -74,7 +78,9 @@ constexpr int kRescaleSlack = 8;
 
 // P8: the FP8 P/V variant -- E4M3 probability codes and MXFP8 V, one byte
 // per key, so V, P and the ones tile take twice the bytes of the E2M1 form.
-template <int D, bool P8 = false>
+// CH: chained slots (causal) -- four query tiles and one K/V tile per slot
+// and stage.
+template <int D, bool P8 = false, bool CH = false>
 struct Layout {
   static constexpr int kRowBytes = D / 2;  // packed E2M1 bytes per Q/K row
   static constexpr int kTileQK = 128 * kRowBytes;
@@ -82,15 +88,19 @@ struct Layout {
   static constexpr int kTileV = D * kKeyBytes;     // D channels x 128 keys
   static constexpr int kTileP = 128 * kKeyBytes;   // 128 query rows x 128 keys
   static constexpr int kSFAtoms = D / 64;          // NVFP4 scale atoms per 128-row tile
-  static constexpr int kQ = 0;                     // two query tiles
-  static constexpr int kK = kQ + 2 * kTileQK;
-  static constexpr int kV = kK + kStages * kTileQK;
-  static constexpr int kP = kV + kStages * kTileV;  // two P tiles
-  static constexpr int kOnes = kP + 2 * kTileP;     // 16 rows of ones (E2M1 or E4M3)
+  static constexpr int kNQ = CH ? 4 : 2;           // query tiles held
+  static constexpr int kNKV = CH ? 2 : 1;          // K/V tiles per ring stage
+  // (the largest form, chained E4M3 with D = 128, fits 227 KB with 2 stages)
+  static constexpr int kStages = (CH && P8 && D == 128) ? 2 : kRingStages;
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + kNQ * kTileQK;
+  static constexpr int kV = kK + kStages * kNKV * kTileQK;
+  static constexpr int kP = kV + kStages * kNKV * kTileV;  // two P tiles
+  static constexpr int kOnes = kP + 2 * kTileP;             // 16 rows of ones (E2M1 or E4M3)
   static constexpr int kSFQ = kOnes + 16 * kKeyBytes;
-  static constexpr int kSFK = kSFQ + 2 * kSFAtoms * 512;
-  static constexpr int kSFV = kSFK + kStages * kSFAtoms * 512;
-  static constexpr int kSFP = kSFV + kStages * 512;
+  static constexpr int kSFK = kSFQ + kNQ * kSFAtoms * 512;
+  static constexpr int kSFV = kSFK + kStages * kNKV * kSFAtoms * 512;
+  static constexpr int kSFP = kSFV + kStages * kNKV * 512;
   static constexpr int kSFOnes = kSFP + 2 * 512;
   static constexpr int kBars = kSFOnes + 512;
   static constexpr int kNumBars = 1 + 2 * kStages + 10;  // q, kv full/empty, s_full/s_free/p_full/o_full/drain x2
@@ -98,7 +108,17 @@ struct Layout {
   static constexpr int kBytes = kMisc + 16;
   // Pad the request so that one CTA owns the SM: it allocates all 512 TMEM columns.
   static constexpr int kAlloc = (kBytes + 1024 > 120 * 1024) ? kBytes + 1024 : 120 * 1024;
+  static_assert(kStages >= 2, "the K/V ring needs at least two stages");
   static_assert(kTileQK % 1024 == 0 && kTileV % 1024 == 0 && kP % 1024 == 0, "tiles keep 1024-B alignment");
+  static_assert(kAlloc <= 227 * 1024, "shared memory of one CTA");
+  // ring buffers of stage s for slot t
+  __host__ __device__ static constexpr int k_of(int s, int t) { return kK + (s * kNKV + (CH ? t : 0)) * kTileQK; }
+  __host__ __device__ static constexpr int v_of(int s, int t) { return kV + (s * kNKV + (CH ? t : 0)) * kTileV; }
+  __host__ __device__ static constexpr int sfk_of(int s, int t) { return kSFK + (s * kNKV + (CH ? t : 0)) * kSFAtoms * 512; }
+  __host__ __device__ static constexpr int sfv_of(int s, int t) { return kSFV + (s * kNKV + (CH ? t : 0)) * 512; }
+  // query tile u (0: first, 1: second of the chain) of slot t
+  __host__ __device__ static constexpr int q_of(int t, int u) { return kQ + (CH ? 2 * t + u : t) * kTileQK; }
+  __host__ __device__ static constexpr int sfq_of(int t, int u) { return kSFQ + (CH ? 2 * t + u : t) * kSFAtoms * 512; }
 };
 
 struct FwdParams {
@@ -130,7 +150,12 @@ template <int D, bool DUMP, bool CAUSAL, bool P8>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_directp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using L = Layout<D, P8>;
+  // Chained slots for the causal E2M1 forward; the causal FP8 P/V forward,
+  // whose doubled K/V tiles would not leave room for a three-stage ring,
+  // pairs query tiles c and T-1-c instead (one tile per slot).
+  constexpr bool kChain = CAUSAL && !P8;
+  using L = Layout<D, P8, kChain>;
+  constexpr int kStages = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
@@ -148,14 +173,75 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.y;
   const int N = p.N;
-  // Query tiles of this CTA and the number of key tiles each consumes (tile
-  // 1 never consumes fewer than tile 0).
-  const int qt0 = CAUSAL ? static_cast<int>(blockIdx.x) : 2 * static_cast<int>(blockIdx.x);
-  const int qt1 = CAUSAL ? p.ntiles - 1 - qt0 : qt0 + 1;
-  const bool has1 = CAUSAL ? qt1 > qt0 : qt1 * 128 < N;  // the second query tile exists
-  const int nkv0 = CAUSAL ? qt0 + 1 : p.ntiles;
-  const int nkv1 = CAUSAL ? qt1 + 1 : p.ntiles;
-  const int nkv = has1 ? nkv1 : nkv0;  // key tiles streamed through the ring
+  // The query tiles of the two slots.  Slot t runs the chain qa[t] (na[t]
+  // key steps) then qb[t] (nb[t] steps, 0 when the chain has one tile); its
+  // key steps are numbered k = 0 .. n_t-1 across the chain.  Slot 1 never
+  // has fewer steps than slot 0.
+  const int T = p.ntiles;
+  int qa0, na0, qb0 = -1, nb0 = 0, qa1 = -1, na1 = 0, qb1 = -1, nb1 = 0;
+  if (!CAUSAL) {
+    qa0 = 2 * static_cast<int>(blockIdx.x);
+    na0 = T;
+    if ((qa0 + 1) * 128 < N) {
+      qa1 = qa0 + 1;
+      na1 = T;
+    }
+  } else if (!kChain) {
+    // query tiles c (c+1 key tiles) and T-1-c (T-c); the second runs alone
+    // once the first is done
+    qa0 = static_cast<int>(blockIdx.x);
+    na0 = qa0 + 1;
+    if (T - 1 - qa0 > qa0) {
+      qa1 = T - 1 - qa0;
+      na1 = T - qa0;
+    }
+  } else {
+    // chain i: query tiles i and T-1-i; for odd T the middle tile alone
+    auto chain = [&](int i, int& qa, int& na, int& qb, int& nb) {
+      qa = i;
+      na = i + 1;
+      if (i < T / 2) {
+        qb = T - 1 - i;
+        nb = T - i;
+      }
+    };
+    const int nchains = (T + 1) / 2;
+    chain(2 * static_cast<int>(blockIdx.x), qa0, na0, qb0, nb0);
+    if (2 * static_cast<int>(blockIdx.x) + 1 < nchains) {
+      chain(2 * static_cast<int>(blockIdx.x) + 1, qa1, na1, qb1, nb1);
+      if (na1 + nb1 < na0 + nb0) {  // the middle tile's short chain goes to slot 0
+        int x = qa0;
+        qa0 = qa1;
+        qa1 = x;
+        x = na0;
+        na0 = na1;
+        na1 = x;
+        x = qb0;
+        qb0 = qb1;
+        qb1 = x;
+        x = nb0;
+        nb0 = nb1;
+        nb1 = x;
+      }
+    }
+  }
+  const bool has1 = na1 > 0;  // the second slot has work
+  const int nkv0 = na0 + nb0, nkv1 = na1 + nb1;
+  const int nkv = has1 ? nkv1 : nkv0;  // key steps streamed through the ring
+  // key step k of slot t: query tile, key tile j within that query tile's
+  // run, the run's length, and which tile of the chain it is
+  struct StepOf {
+    int qt, j, len, u;
+  };
+  auto step_of = [&](int t, int k) -> StepOf {
+    if constexpr (!kChain) {
+      return StepOf{t ? qa1 : qa0, k, t ? na1 : na0, 0};  // one query tile per slot
+    } else {
+      const int na = t ? na1 : na0;
+      if (k < na) return StepOf{t ? qa1 : qa0, k, na, 0};
+      return StepOf{t ? qb1 : qb0, k - na, t ? nb1 : nb0, 1};
+    }
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q_full, 1);
@@ -206,38 +292,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      mbar_arrive_expect_tx(bar_q_full, (has1 ? 2 : 1) * (L::kTileQK + kSfBytes));
-      for (int t = 0; t < (has1 ? 2 : 1); ++t) {
-        const int qt = t ? qt1 : qt0;
-        tma_load_3d(smem + L::kQ + t * L::kTileQK, &tm_q, bar_q_full, 0, qt * 128, bh);
-        bulk_load(smem + L::kSFQ + t * kSfBytes, p.q_sf + (static_cast<size_t>(bh) * p.ntiles + qt) * kSfBytes,
-                  kSfBytes, bar_q_full);
+      // every query tile of both slots, with its scale atoms
+      int nq = has1 ? 2 : 1;
+      if constexpr (kChain) {
+        nq = 0;
+        for (int t = 0; t < 2; ++t)
+          for (int u = 0; u < 2; ++u) nq += ((u ? (t ? nb1 : nb0) : (t ? na1 : na0)) > 0) ? 1 : 0;
       }
+      mbar_arrive_expect_tx(bar_q_full, nq * (L::kTileQK + kSfBytes));
+      for (int t = 0; t < 2; ++t)
+        for (int u = 0; u < 2; ++u) {
+          if ((u ? (t ? nb1 : nb0) : (t ? na1 : na0)) == 0) continue;
+          const int qt = u ? (t ? qb1 : qb0) : (t ? qa1 : qa0);
+          tma_load_3d(smem + L::q_of(t, u), &tm_q, bar_q_full, 0, qt * 128, bh);
+          bulk_load(smem + L::sfq_of(t, u), p.q_sf + (static_cast<size_t>(bh) * T + qt) * kSfBytes, kSfBytes,
+                    bar_q_full);
+        }
     }
-    int issued = 0;  // key/value tiles whose copies were issued
-    for (int j = 0; j < nkv; ++j) {
-      const int s = j % kStages;
-      if (j >= kStages) {
-        const bool ok = mbar_wait(bar_kv_empty + s, ((j / kStages) - 1) & 1, abort_flag, p.status, 1);
+    int issued = 0;  // key steps whose copies were issued
+    for (int k = 0; k < nkv; ++k) {
+      const int s = k % kStages;
+      if (k >= kStages) {
+        const bool ok = mbar_wait(bar_kv_empty + s, ((k / kStages) - 1) & 1, abort_flag, p.status, 1);
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
       }
       if (leader) {
-        mbar_arrive_expect_tx(bar_kv_full + s, L::kTileQK + L::kTileV + kSfBytes + 512);
-        tma_load_3d(smem + L::kK + s * L::kTileQK, &tm_k, bar_kv_full + s, 0, j * 128, bh);
-        tma_load_2d(smem + L::kV + s * L::kTileV, &tm_v, bar_kv_full + s, j * L::kKeyBytes, bh * D);
-        bulk_load(smem + L::kSFK + s * kSfBytes, p.k_sf + (static_cast<size_t>(bh) * p.ntiles + j) * kSfBytes,
-                  kSfBytes, bar_kv_full + s);
-        bulk_load(smem + L::kSFV + s * 512, p.v_sf + (static_cast<size_t>(bh) * p.ntiles + j) * 512, 512,
-                  bar_kv_full + s);
+        // the key tile of each slot that takes step k (chained slots: one
+        // each; otherwise the slots share one)
+        if constexpr (!kChain) {
+          mbar_arrive_expect_tx(bar_kv_full + s, L::kTileQK + L::kTileV + kSfBytes + 512);
+          tma_load_3d(smem + L::kK + s * L::kTileQK, &tm_k, bar_kv_full + s, 0, k * 128, bh);
+          tma_load_2d(smem + L::kV + s * L::kTileV, &tm_v, bar_kv_full + s, k * L::kKeyBytes, bh * D);
+          bulk_load(smem + L::kSFK + s * kSfBytes, p.k_sf + (static_cast<size_t>(bh) * T + k) * kSfBytes, kSfBytes,
+                    bar_kv_full + s);
+          bulk_load(smem + L::kSFV + s * 512, p.v_sf + (static_cast<size_t>(bh) * T + k) * 512, 512, bar_kv_full + s);
+        }
+        const int nslots = kChain ? ((k < nkv0 ? 1 : 0) + (has1 && k < nkv1 ? 1 : 0)) : 1;
+        if (kChain) mbar_arrive_expect_tx(bar_kv_full + s, nslots * (L::kTileQK + L::kTileV + kSfBytes + 512));
+        for (int t = 0; t < (kChain ? 2 : 0); ++t) {
+          if (kChain && k >= (t ? (has1 ? nkv1 : 0) : nkv0)) continue;
+          const int j = kChain ? step_of(t, k).j : k;
+          tma_load_3d(smem + L::k_of(s, t), &tm_k, bar_kv_full + s, 0, j * 128, bh);
+          tma_load_2d(smem + L::v_of(s, t), &tm_v, bar_kv_full + s, j * L::kKeyBytes, bh * D);
+          bulk_load(smem + L::sfk_of(s, t), p.k_sf + (static_cast<size_t>(bh) * T + j) * kSfBytes, kSfBytes,
+                    bar_kv_full + s);
+          bulk_load(smem + L::sfv_of(s, t), p.v_sf + (static_cast<size_t>(bh) * T + j) * 512, 512,
+                    bar_kv_full + s);
+        }
       }
-      issued = j + 1;
+      issued = k + 1;
       __syncwarp();
     }
     // Before leaving, make sure no copy into this CTA's shared memory is
     // still in flight, even when the CTA is giving up: wait for the last
     // issued fill of every stage.
-    for (int j = issued - kStages < 0 ? 0 : issued - kStages; j < issued; ++j)
-      mbar_wait_drain(bar_kv_full + (j % kStages), (j / kStages) & 1, abort_flag, p.status, 2);
+    for (int k = issued - kStages < 0 ? 0 : issued - kStages; k < issued; ++k)
+      mbar_wait_drain(bar_kv_full + (k % kStages), (k / kStages) & 1, abort_flag, p.status, 2);
     mbar_wait_drain(bar_q_full, 0, abort_flag, p.status, 3);
   } else if (warp == kWarpMma0 || (warp == kWarpMma0 + 1 && has1)) {
     // ------------------------------------------------------------ MMA issuers
@@ -260,12 +370,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Descriptors are built once; the start-address field is linear in the
     // shared-memory address (16-byte units), so tiles are reached by adding
     // their offset.
-    const uint64_t qdesc = smem_desc(smem_u32(smem + L::kQ + t * L::kTileQK), 16, kSbo, kSwizzleQK);
-    const uint64_t kdesc0 = smem_desc(smem_u32(smem + L::kK), 16, kSbo, kSwizzleQK);
-    const uint64_t vdesc0 = smem_desc(smem_u32(smem + L::kV), 16, kSboKV, kSwizzleKV);
+    const uint64_t qdesc_a = smem_desc(smem_u32(smem + L::q_of(t, 0)), 16, kSbo, kSwizzleQK);
+    const uint64_t qdesc_b = smem_desc(smem_u32(smem + L::q_of(t, 1)), 16, kSbo, kSwizzleQK);
+    const uint64_t kdesc0 = smem_desc(smem_u32(smem + L::k_of(0, t)), 16, kSbo, kSwizzleQK);
+    const uint64_t vdesc0 = smem_desc(smem_u32(smem + L::v_of(0, t)), 16, kSboKV, kSwizzleKV);
     const uint64_t pdesc = smem_desc(smem_u32(smem + L::kP + t * L::kTileP), 16, kSboKV, kSwizzleKV);
     const uint64_t ones_desc = smem_desc(smem_u32(smem + L::kOnes), 16, kSboKV, kSwizzleKV);
-    constexpr uint64_t kQKStep = L::kTileQK >> 4, kVStep = L::kTileV >> 4;
+    // ring stages are kNKV tiles apart
+    constexpr uint64_t kQKStep = (L::kNKV * L::kTileQK) >> 4, kVStep = (L::kNKV * L::kTileV) >> 4;
     const uint32_t t_s = tmem + kColS;
     const uint32_t t_o = tmem + kColO + t * D;
     const uint32_t t_l = tmem + kColL + 16 * t;
@@ -293,25 +405,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       return wait(bar_s_free + (has1 ? 1 : 0), (j - 1) & 1, 13);
     };
     // The whole warp runs each issue; one elected lane issues (inside the asm).
-    const uint32_t sfk_src = smem_u32(smem + L::kSFK), sfv_src = smem_u32(smem + L::kSFV);
+    const uint32_t sfk_src = smem_u32(smem + L::sfk_of(0, t)), sfv_src = smem_u32(smem + L::sfv_of(0, t));
     const uint32_t sfp_src = smem_u32(smem + L::kSFP + t * 512);
-    auto issue_qk = [&](int j) {  // K scale atoms of step j, then S = Q_t K(j)^T
-      const int s = j % kStages;
-      const uint32_t sfk = t_sfk + 8 * (j & 1);
+    constexpr uint32_t kSfkStep = L::kNKV * L::kSFAtoms * 512, kSfvStep = L::kNKV * 512;
+    auto issue_qk = [&](int k) {  // K scale atoms of step k, then S = Q K(j)^T for the step's query tile
+      const int s = k % kStages;
+      const StepOf st = step_of(t, k);
+      if (kChain && k > 0 && st.j == 0) {
+        // the chain moves on to its second query tile: its Q scale atoms
+        // replace the first tile's (after that tile's products, in issue order)
+        for (int a = 0; a < L::kSFAtoms; ++a)
+          tc_cp_sf_atom_warp(t_sfq + 4 * a, smem_u32(smem + L::sfq_of(t, 1) + a * 512));
+      }
+      const uint64_t qdesc = st.u ? qdesc_b : qdesc_a;
+      const uint32_t sfk = t_sfk + 8 * (k & 1);
 #pragma unroll
-      for (int a = 0; a < L::kSFAtoms; ++a) tc_cp_sf_atom_warp(sfk + 4 * a, sfk_src + (s * L::kSFAtoms + a) * 512);
+      for (int a = 0; a < L::kSFAtoms; ++a) tc_cp_sf_atom_warp(sfk + 4 * a, sfk_src + s * kSfkStep + a * 512);
 #pragma unroll
       for (int ks = 0; ks < D / 64; ++ks)
         mma_nvf4_warp(t_s, qdesc + 2 * ks, kdesc0 + s * kQKStep + 2 * ks, idesc_qk, t_sfq + 4 * ks, sfk + 4 * ks,
                       ks > 0);
       tc_commit_warp(s_full);
     };
-    auto issue_pv = [&](int j) {  // P and V scale atoms, O_t += P_t V(j), l_t = P_t 1
-      const int s = j % kStages;
-      const uint32_t sfv = t_sfv + 4 * (j & 1);
+    auto issue_pv = [&](int k) {  // P and V scale atoms, O_t += P_t V(j), l_t = P_t 1
+      const int s = k % kStages;
+      const int j = step_of(t, k).j;  // 0: the first product of a query tile overwrites O
+      const uint32_t sfv = t_sfv + 4 * (k & 1);
       const uint64_t vd = vdesc0 + s * kVStep;
       tc_cp_sf_atom_warp(t_sfp, sfp_src);
-      tc_cp_sf_atom_warp(sfv, sfv_src + s * 512);
+      tc_cp_sf_atom_warp(sfv, sfv_src + s * kSfvStep);
       if constexpr (P8) {
         // E4M3 operands: four K = 32 products per 128 keys, each with the
         // scale byte k of its 32-key block (one scale per row and block)
@@ -331,15 +453,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_commit_warp(o_full);
       tc_commit_warp(bar_kv_empty + s);
-      // a stage that tile 0 does not consume still needs both releases
-      if (t == 1 && j >= nkv0) tc_commit_warp(bar_kv_empty + s);
+      // a stage that slot 0 does not consume still needs both releases
+      if (t == 1 && k >= nkv0) tc_commit_warp(bar_kv_empty + s);
     };
 
     bool ok = wait(bar_q_full, 0, 10);
     if (ok) {
       tc_fence_after();
       for (int a = 0; a < L::kSFAtoms; ++a)
-        tc_cp_sf_atom_warp(t_sfq + 4 * a, smem_u32(smem + L::kSFQ + (t * L::kSFAtoms + a) * 512));
+        tc_cp_sf_atom_warp(t_sfq + 4 * a, smem_u32(smem + L::sfq_of(t, 0) + a * 512));
       tc_cp_sf_atom_warp(t_sf1, smem_u32(smem + L::kSFOnes));
       ok = wait(bar_kv_full, 0, 11);
     }
@@ -348,18 +470,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       issue_qk(0);
     }
-    // Per KV step j: the next scores first (they need only K(j+1) and the
-    // bank), then this tile's PV product of step j.
-    for (int j = 0; ok && j < nkv_t; ++j) {
-      if (j + 1 < nkv_t) {
-        if (!(ok = wait(bar_kv_full + (j + 1) % kStages, ((j + 1) / kStages) & 1, 14))) break;
-        if (!(ok = bank_free(j + 1))) break;
+    // Per key step k: the next scores first (they need only the next key
+    // tile and the bank), then this slot's PV product of step k.
+    for (int k = 0; ok && k < nkv_t; ++k) {
+      if (k + 1 < nkv_t) {
+        if (!(ok = wait(bar_kv_full + (k + 1) % kStages, ((k + 1) / kStages) & 1, 14))) break;
+        if (!(ok = bank_free(k + 1))) break;
         tc_fence_after();
-        issue_qk(j + 1);
+        issue_qk(k + 1);
       }
-      if (!(ok = wait(p_full, j & 1, 15))) break;
+      if (!(ok = wait(p_full, k & 1, 15))) break;
       tc_fence_after();
-      issue_pv(j);
+      issue_pv(k);
     }
     // Every MMA and scale copy this warp issued must have completed before
     // TMEM is freed, even when the CTA is giving up.
@@ -367,10 +489,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait_drain(bar_drain + t, 0, abort_flag, p.status, 17);
   } else if (warp < 8 && (warp < 4 || has1)) {
     // ------------------------------------------------------------ softmax rows
-    const int t = warp >> 2;            // query tile of this warpgroup
+    const int t = warp >> 2;            // slot of this warpgroup
     const int row = threadIdx.x & 127;  // == TMEM lane
-    const int qrow = (t ? qt1 : qt0) * 128 + row;
     const int nkv_t = t ? nkv1 : nkv0;
+    int qrow = (t ? qa1 : qa0) * 128 + row;  // query row of the current tile
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + kColS;
     const uint32_t tO = tmem + lane_base + kColO + t * D;
@@ -383,14 +505,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sSFP = smem + L::kSFP + t * 512;
     const float c = static_cast<float>(((static_cast<double>(p.softmax_scale) * kLog2E) *
                                         static_cast<double>(*p.g_q)) * static_cast<double>(*p.g_k));
-    const bool dump_row = DUMP && bh == p.dump_bh && qrow >= p.dump_row0 && qrow < p.dump_row0 + p.dump_nrows;
+    auto is_dump_row = [&](int qr) {
+      return DUMP && bh == p.dump_bh && qr >= p.dump_row0 && qr < p.dump_row0 + p.dump_nrows;
+    };
+    // O / l of the current query tile's row -> bf16 O and the LSE (the whole
+    // warp reads the output bank: tcgen05.ld is warp-collective)
+    auto write_out = [&](int qr, int m_e, float l_e) {
+      const float inv_l = 1.0f / l_e;
+      const bool store = qr < N;
+      const bool dump = is_dump_row(qr);
+      __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * N + (store ? qr : 0)) * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        float o[32];
+        tmem_ld32(tO + 32 * cc, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] *= inv_l;
+        if (store) {
+          uint32_t packed[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+            packed[i] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * cc);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+        }
+        if (dump) {
+          float* od = p.dump_o + static_cast<size_t>(qr - p.dump_row0) * D + 32 * cc;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) od[i] = o[i];
+        }
+      }
+      if (store) p.lse[static_cast<size_t>(bh) * N + qr] = 0.69314718055994531f * (static_cast<float>(m_e) + log2f(l_e));
+    };
     int m_ref = 0;
     float l_run = 0.0f;  // denominator, relative to 2^m_ref
     bool ok = true;
     // tcgen05.ld / tcgen05.st are warp-collective (.sync.aligned): every
     // branch around them below is made warp-uniform with a vote.
-    for (int j = 0; j < nkv_t; ++j) {
-      ok = mbar_wait(s_full, j & 1, abort_flag, p.status, 20);
+    for (int k = 0; k < nkv_t; ++k) {
+      const StepOf st = step_of(t, k);
+      const int j = st.j;             // key tile within the current query tile's run
+      const int qrow_prev = qrow;     // the previous query tile's row, at a switch
+      if (kChain) qrow = st.qt * 128 + row;
+      const bool dump_row = is_dump_row(qrow);
+      ok = mbar_wait(s_full, k & 1, abort_flag, p.status, 20);
       if (!__all_sync(0xFFFFFFFFu, ok)) {
         ok = false;
         break;
@@ -411,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       int valid = N - j * 128;  // keys of this tile that exist (>= 1)
       // causal: on the diagonal tile (the last one) row r sees keys 0 .. r
-      if (CAUSAL && j == nkv_t - 1) valid = min(valid, row + 1);
+      if (CAUSAL && j == st.len - 1) valid = min(valid, row + 1);
       if (valid < 128) {
         // partial tile: keys past N (or past the diagonal) are masked and the
         // maxima retaken
@@ -437,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         kb[b] = (xb[b] == -INFINITY) ? 0 : static_cast<int>(ceilf(__fsub_rn(xb[b], P8 ? kLog2_448 : kLog2Six)));
       }
       const int m_tile = static_cast<int>(ceilf(xmax));
-      const int m_old = m_ref;
+      const int m_old = m_ref;  // also the previous query tile's reference at a switch
       bool rescale = false;
       if (j == 0) {
         m_ref = m_tile;
@@ -477,14 +640,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the O / l banks are touched; it normally finished long ago.  Its tile
       // denominator (relative to the reference it was made with) joins l.
       float l_prev = 0.0f;
-      if (j > 0) {
-        ok = mbar_wait(o_full, (j - 1) & 1, abort_flag, p.status, 21);
+      if (k > 0) {
+        ok = mbar_wait(o_full, (k - 1) & 1, abort_flag, p.status, 21);
         if (!__all_sync(0xFFFFFFFFu, ok)) {
           ok = false;
           break;
         }
         tc_fence_after();
         l_prev = tmem_ld1(tL);  // completes at a wait below
+        if (kChain && j == 0) {
+          // the chain has moved on to its second query tile: the first one's
+          // products are all complete -- write its O and LSE out before this
+          // step's PV product overwrites the output bank
+          tmem_wait_ld();
+          write_out(qrow_prev, m_old, l_run + l_prev);
+          l_run = 0.0f;
+          l_prev = 0.0f;
+        }
       }
       // Rescale O of the rows whose reference maximum moved; the whole warp
       // takes part in the TMEM round trip, other rows multiply by 1.
@@ -515,11 +687,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<uint32_t*>(sSFP + (row & 31) * 16 + (row >> 5) * 4) = sfword;
       if (dump_row) {
         const size_t rr = static_cast<size_t>(qrow - p.dump_row0);
-        uint4* dst = reinterpret_cast<uint4*>(p.dump_codes + rr * (p.ntiles * L::kKeyBytes) + j * L::kKeyBytes);
+        uint4* dst = reinterpret_cast<uint4*>(p.dump_codes + rr * (T * L::kKeyBytes) + j * L::kKeyBytes);
 #pragma unroll
         for (int u = 0; u < kWords / 4; ++u) dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
 #pragma unroll
-        for (int b = 0; b < 4; ++b) p.dump_kshift[rr * (p.ntiles * 4) + j * 4 + b] = kb[b];
+        for (int b = 0; b < 4; ++b) p.dump_kshift[rr * (T * 4) + j * 4 + b] = kb[b];
       }
       tmem_wait_ld();
       l_run += l_prev;
@@ -534,36 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float l = l_run + tmem_ld1(tL);
       tmem_wait_ld();
-      const float inv_l = 1.0f / l;
-      const bool store = qrow < N;
-      __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * N + (store ? qrow : 0)) * D;
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        float o[32];
-        tmem_ld32(tO + 32 * cc, o);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] *= inv_l;
-        if (store) {
-          uint32_t packed[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
-            packed[i] = *reinterpret_cast<uint32_t*>(&h2);
-          }
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * cc);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
-        }
-        if (dump_row) {
-          float* od = p.dump_o + static_cast<size_t>(qrow - p.dump_row0) * D + 32 * cc;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) od[i] = o[i];
-        }
-      }
-      if (store)
-        p.lse[static_cast<size_t>(bh) * N + qrow] = 0.69314718055994531f * (static_cast<float>(m_ref) + log2f(l));
+      write_out(qrow, m_ref, l);
     }
   }
 
@@ -607,7 +750,7 @@ template <int D, bool DUMP, bool CAUSAL = false, bool P8 = false>
 int launch(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k, const fp4attn_mxfp4_t* v, void* o, float* lse,
            int B, int H, int N, float softmax_scale, int dump_bh, int row0, int nrows, uint8_t* codes,
            int32_t* kshift, float* o_f32, cudaStream_t stream, DeviceStatus* status_word = nullptr) {
-  using L = Layout<D, P8>;
+  using L = Layout<D, P8, CAUSAL && !P8>;
   DeviceStatus* status = status_word ? status_word : device_status_ptr();
   if (!status) return FP4ATTN_ERR_CUDA;
   const int ntiles = n_row_tiles(N);
@@ -653,8 +796,11 @@ int launch(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k, const fp4attn_mxf
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   });
   if (attr_err != cudaSuccess) return FP4ATTN_ERR_CUDA;
-  // two query tiles per CTA: (2c, 2c+1), or causal (c, ntiles-1-c)
-  dim3 grid((ntiles + 1) / 2, BH);
+  // two query tiles per CTA: (2c, 2c+1); causal E2M1: two chains of two
+  // query tiles (the middle tile of an odd count alone); causal FP8 P/V:
+  // (c, ntiles-1-c)
+  const int nchains = (ntiles + 1) / 2;
+  dim3 grid((CAUSAL && !P8) ? (nchains + 1) / 2 : (ntiles + 1) / 2, BH);
   kern<<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, prm);
   return cuda_status(cudaGetLastError());
 }
