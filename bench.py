@@ -53,10 +53,10 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic of one forward launch, from an ncu capture (see profiles/), and
 # the hash of the kernel sources it was taken on; reported only while the
 # sources are unchanged.
-TRAFFIC_RECORD = {"sources_sha": "921ec241564feee3", "bytes_per_launch": 278377984 + 291709440,
+TRAFFIC_RECORD = {"sources_sha": "7c860c7f45c7b1ad", "bytes_per_launch": 279551744 + 291830784,
                   "note": "dram__bytes_read.sum + dram__bytes_write.sum of one launch on the 40-head "
                           "N=32768 D=128 workload (profiles/fwd_directp_B1_H40_N32768_D128_traffic.md)"}
-TRAFFIC_RECORD_CAUSAL = {"sources_sha": TRAFFIC_RECORD["sources_sha"], "bytes_per_launch": 278469632 + 292907008,
+TRAFFIC_RECORD_CAUSAL = {"sources_sha": TRAFFIC_RECORD["sources_sha"], "bytes_per_launch": 278415872 + 293369600,
                          "note": "the same capture of the causal forward "
                                  "(profiles/fwd_directp_B1_H40_N32768_D128_traffic.md)"}
 KERNEL_SOURCES = ["blackwell_nvfp4_quantize_gb300/csrc/fwd_directp.cu", "blackwell_nvfp4_quantize_gb300/csrc/ptx.cuh"]
