@@ -30,6 +30,16 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
   return __uint_as_float(((e + 120u) << 23) | (m << 20));
 }
 
+// 16-byte load of data read once: not kept in L1, with a 256-byte L2
+// prefetch so each DRAM burst brings whole lines the neighbouring lanes use.
+__device__ __forceinline__ uint4 ld_stream(const uint4* ptr) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr));
+  return v;
+}
+
 __device__ __forceinline__ float global_scale(float amax) {
   return amax > 0.0f ? __fdiv_rn(amax, kNvfp4GlobalDiv) : 1.0f;
 }
@@ -48,15 +58,14 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint4* __restrict__ x, 
   uint32_t m2 = 0;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (; i + 3 * stride < nvec; i += 4 * stride) {
-    const uint4 a = __ldcs(x + i), b = __ldcs(x + i + stride), c = __ldcs(x + i + 2 * stride),
-                d = __ldcs(x + i + 3 * stride);
-    m2 = absmax_vec(a, m2);
-    m2 = absmax_vec(b, m2);
-    m2 = absmax_vec(c, m2);
-    m2 = absmax_vec(d, m2);
+  for (; i + 7 * stride < nvec; i += 8 * stride) {
+    uint4 a[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) a[u] = ld_stream(x + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) m2 = absmax_vec(a[u], m2);
   }
-  for (; i < nvec; i += stride) m2 = absmax_vec(__ldcs(x + i), m2);
+  for (; i < nvec; i += stride) m2 = absmax_vec(ld_stream(x + i), m2);
   uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
   m = __reduce_max_sync(0xFFFFFFFFu, m);
   __shared__ uint32_t red[8];
@@ -87,7 +96,7 @@ __global__ void __launch_bounds__(256) nvfp4_quant_kernel(const uint4* __restric
     const bool active = blk < nblocks;
     uint32_t sb = 0;
     if (active) {
-      const uint4 a = __ldcs(x + 2 * blk), b = __ldcs(x + 2 * blk + 1);
+      const uint4 a = ld_stream(x + 2 * blk), b = ld_stream(x + 2 * blk + 1);
       uint32_t m2 = absmax_vec(b, absmax_vec(a, 0u));
       const float amax_b = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
       sb = cvt_e4m3(__fdiv_rn(amax_b, six_g));
@@ -143,7 +152,7 @@ __global__ void __launch_bounds__(256) mxfp4_v_kernel(const uint4* __restrict__ 
     const int r = i / VPR, cv = i % VPR;
     const int n = kt * 128 + r;
     uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (n < N) val = __ldcs(v + ((bh * N + n) * VPR + cv));
+    if (n < N) val = ld_stream(v + ((bh * N + n) * VPR + cv));
     *reinterpret_cast<uint4*>(&tile[r * D + cv * 8]) = val;
   }
   if (threadIdx.x < 128) atom[threadIdx.x] = 0u;
@@ -195,7 +204,7 @@ __global__ void __launch_bounds__(256) mxfp8_v_kernel(const uint4* __restrict__ 
     const int r = i / VPR, cv = i % VPR;
     const int n = kt * 128 + r;
     uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (n < N) val = __ldcs(v + ((bh * N + n) * VPR + cv));
+    if (n < N) val = ld_stream(v + ((bh * N + n) * VPR + cv));
     *reinterpret_cast<uint4*>(&tile[r * D + cv * 8]) = val;
   }
   if (threadIdx.x < 128) atom[threadIdx.x] = 0u;
