@@ -74,3 +74,31 @@ def test_timeout_status_word_is_clear():
     import blackwell_nvfp4_quantize_gb300 as fa
 
     assert fa.device_status() == fa.FP4ATTN_OK
+
+
+def test_side_streams_and_preallocated_outputs():
+    # every call is asynchronous on the caller's stream: two forwards on two
+    # side streams at once, into preallocated outputs, give the results of the
+    # default-stream call
+    import torch
+
+    import blackwell_nvfp4_quantize_gb300 as fa
+
+    q, k, v = wl.make_custom(1, 4, 1000, 128, seed=77, kind="normal", scale=1.5)
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    o_ref, lse_ref = fa.attention(qc, kc, vc)
+    oc_ref, lsec_ref = fa.attention(qc, kc, vc, causal=True)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    o1, o2 = torch.empty_like(o_ref), torch.empty_like(o_ref)
+    l1, l2 = torch.empty_like(lse_ref), torch.empty_like(lse_ref)
+    with torch.cuda.stream(s1):
+        q1, k1, v1 = fa.quant_qk_nvfp4(qc, stream=s1), fa.quant_qk_nvfp4(kc, stream=s1), fa.quant_v_mxfp4(vc, stream=s1)
+        fa.fwd_directp(q1, k1, v1, o=o1, lse=l1, stream=s1)
+    with torch.cuda.stream(s2):
+        q2, k2, v2 = fa.quant_qk_nvfp4(qc, stream=s2), fa.quant_qk_nvfp4(kc, stream=s2), fa.quant_v_mxfp4(vc, stream=s2)
+        fa.fwd_directp_causal(q2, k2, v2, o=o2, lse=l2, stream=s2)
+    torch.cuda.synchronize()
+    assert fa.device_status() == fa.FP4ATTN_OK
+    assert torch.equal(o1, o_ref) and torch.equal(l1, lse_ref)
+    assert torch.equal(o2, oc_ref) and torch.equal(l2, lsec_ref)
