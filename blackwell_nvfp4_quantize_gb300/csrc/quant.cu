@@ -11,9 +11,10 @@
 //                       training keeps FP8 probabilities and values), one
 //                       byte per key
 //
-// All three data kernels are HBM-bound streaming passes: 16-byte vector loads,
-// grid sized in multiples of the SM count, warp-shuffle reductions, and
-// coalesced stores.  fp32 arithmetic uses explicitly rounded intrinsics so that
+// The data kernels are HBM-bound streaming passes: 16-byte vector loads with
+// 4 to 16 of them in flight per thread (a read stream on this GPU needs about
+// 8 to approach the DRAM peak), grids in multiples of the SM count,
+// warp-shuffle reductions and coalesced stores.  fp32 arithmetic uses explicitly rounded intrinsics so that
 // no multiply-add contraction changes a code.
 #include <cuda_bf16.h>
 
@@ -53,19 +54,26 @@ __device__ __forceinline__ uint32_t absmax_vec(const uint4& v, uint32_t m2) {
   return m2;
 }
 
+// Each warp streams contiguous chunks of 32 * kAmaxUnroll vectors (8 KB),
+// all of a chunk's loads in flight at once; chunks go round-robin over warps.
+constexpr int kAmaxUnroll = 16;
+
 __global__ void __launch_bounds__(256) amax_kernel(const uint4* __restrict__ x, long long nvec,
                                                    unsigned int* __restrict__ amax_bits) {
   uint32_t m2 = 0;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (; i + 7 * stride < nvec; i += 8 * stride) {
-    uint4 a[8];
+  const int lane = threadIdx.x & 31;
+  constexpr long long kChunk = 32ll * kAmaxUnroll;
+  const long long wstride = static_cast<long long>(gridDim.x) * blockDim.x * kAmaxUnroll;
+  long long base = (static_cast<long long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31)) * kAmaxUnroll;
+  for (; base + kChunk <= nvec; base += wstride) {
+    uint4 a[kAmaxUnroll];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) a[u] = ld_stream(x + i + u * stride);
+    for (int u = 0; u < kAmaxUnroll; ++u) a[u] = ld_stream(x + base + 32 * u + lane);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) m2 = absmax_vec(a[u], m2);
+    for (int u = 0; u < kAmaxUnroll; ++u) m2 = absmax_vec(a[u], m2);
   }
-  for (; i < nvec; i += stride) m2 = absmax_vec(ld_stream(x + i), m2);
+  // the partial last chunk falls to the one warp whose turn it is
+  for (long long i = base + lane; i < nvec; i += 32) m2 = absmax_vec(ld_stream(x + i), m2);
   uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
   m = __reduce_max_sync(0xFFFFFFFFu, m);
   __shared__ uint32_t red[8];
@@ -80,59 +88,106 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint4* __restrict__ x, 
 }
 
 // One thread per 16-element block; a warp covers 32 consecutive blocks, so
-// the 4 scale bytes of one atom word come from 4 neighbouring lanes.
+// the 4 scale bytes of one atom word come from 4 neighbouring lanes.  Each
+// warp takes kQuantUnroll such groups (4 KB of input) at a time, with all of
+// their loads in flight before the first block is encoded.
+constexpr int kQuantUnroll = 4;
+
 __global__ void __launch_bounds__(256) nvfp4_quant_kernel(const uint4* __restrict__ x, uint2* __restrict__ payload,
                                                           uint8_t* __restrict__ sf, const float* __restrict__ amax_in,
                                                           int N, int D, long long nblocks) {
   const float g = global_scale(*amax_in);
   const float six_g = __fmul_rn(6.0f, g);
-  const int kbs = D / 16;
+  const int kbs = D / 16;  // 4 or 8 blocks per row
+  const int kbs_log2 = (D == 128) ? 3 : 2;
   const int ntiles = (N + 127) / 128;
   const int lane = threadIdx.x & 31;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long base = static_cast<long long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
-       base < nblocks; base += stride) {
-    const long long blk = base + lane;
-    const bool active = blk < nblocks;
-    uint32_t sb = 0;
-    if (active) {
-      const uint4 a = ld_stream(x + 2 * blk), b = ld_stream(x + 2 * blk + 1);
-      uint32_t m2 = absmax_vec(b, absmax_vec(a, 0u));
-      const float amax_b = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
-      sb = cvt_e4m3(__fdiv_rn(amax_b, six_g));
-      const float s = __fmul_rn(e4m3_value(sb), g);
-      uint2 out = make_uint2(0u, 0u);
-      if (s != 0.0f) {
-        const float inv = __frcp_rn(s);
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        float y[16];
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x * kQuantUnroll;
+  for (long long base0 = (static_cast<long long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31)) * kQuantUnroll;
+       base0 < nblocks; base0 += stride) {
+    uint4 va[kQuantUnroll], vb[kQuantUnroll];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          y[2 * k] = __fmul_rn(__uint_as_float(w[k] << 16), inv);
-          y[2 * k + 1] = __fmul_rn(__uint_as_float(w[k] & 0xFFFF0000u), inv);
-        }
-        out.x = cvt_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
-        out.y = cvt_e2m1x8(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]);
+    for (int u = 0; u < kQuantUnroll; ++u) {
+      const long long blk = base0 + 32 * u + lane;
+      if (blk < nblocks) {
+        va[u] = ld_stream(x + 2 * blk);
+        vb[u] = ld_stream(x + 2 * blk + 1);
       }
-      __stcs(payload + blk, out);
     }
-    // gather the four scale bytes of one atom word into the lane with k == 0
-    uint32_t word = sb << (8 * (lane & 3));
-    word |= __shfl_xor_sync(0xFFFFFFFFu, word, 1);
-    word |= __shfl_xor_sync(0xFFFFFFFFu, word, 2);
-    if (active && (lane & 3) == 0) {
-      const long long row = blk / kbs;
-      const int kb = static_cast<int>(blk % kbs);
-      const long long bh = row / N;
-      const int n = static_cast<int>(row % N);
-      const int r = n & 127;
-      const long long atom = (bh * ntiles + n / 128) * (kbs / 4) + kb / 4;
-      *reinterpret_cast<uint32_t*>(sf + atom * 512 + (r & 31) * 16 + (r >> 5) * 4) = word;
+#pragma unroll
+    for (int u = 0; u < kQuantUnroll; ++u) {
+      const long long blk = base0 + 32 * u + lane;
+      const bool active = blk < nblocks;
+      uint32_t sb = 0;
+      if (active) {
+        const uint4 a = va[u], b = vb[u];
+        uint32_t m2 = absmax_vec(b, absmax_vec(a, 0u));
+        const float amax_b = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
+        sb = cvt_e4m3(__fdiv_rn(amax_b, six_g));
+        const float s = __fmul_rn(e4m3_value(sb), g);
+        uint2 out = make_uint2(0u, 0u);
+        if (s != 0.0f) {
+          const float inv = __frcp_rn(s);
+          const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+          float y[16];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            y[2 * k] = __fmul_rn(__uint_as_float(w[k] << 16), inv);
+            y[2 * k + 1] = __fmul_rn(__uint_as_float(w[k] & 0xFFFF0000u), inv);
+          }
+          out.x = cvt_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
+          out.y = cvt_e2m1x8(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]);
+        }
+        __stcs(payload + blk, out);
+      }
+      // gather the four scale bytes of one atom word into the lane with k == 0
+      uint32_t word = sb << (8 * (lane & 3));
+      word |= __shfl_xor_sync(0xFFFFFFFFu, word, 1);
+      word |= __shfl_xor_sync(0xFFFFFFFFu, word, 2);
+      if (active && (lane & 3) == 0) {
+        // row = (b*H + h)*N + n < 2^31; for N a multiple of 128 the row's
+        // 128-row tile index is row / 128 without splitting off the head
+        const int row = static_cast<int>(blk >> kbs_log2);
+        const int kb = static_cast<int>(blk) & (kbs - 1);
+        long long tile;
+        int r;
+        if ((N & 127) == 0) {
+          tile = row >> 7;
+          r = row & 127;
+        } else {
+          const int bh = row / N, n = row - bh * N;
+          tile = static_cast<long long>(bh) * ntiles + (n >> 7);
+          r = n & 127;
+        }
+        const long long atom = tile * (kbs / 4) + (kb >> 2);
+        *reinterpret_cast<uint32_t*>(sf + atom * 512 + (r & 31) * 16 + (r >> 5) * 4) = word;
+      }
     }
   }
 }
 
 __global__ void nvfp4_finalize_kernel(float* g) { *g = global_scale(*g); }
+
+// The 128 token rows of key tile kt of head bh (rows past N as zeros) into
+// shared memory, row-major: the tile is one contiguous stretch of V, and each
+// of the 256 threads has all of its 16-byte loads in flight before its first
+// store.
+template <int D>
+__device__ __forceinline__ void stage_v_tile(const uint4* __restrict__ v, uint16_t* tile, int kt, long long bh,
+                                             int N) {
+  constexpr int VPR = D / 8;                   // 16-byte vectors per token row
+  constexpr int kPerThread = 128 * VPR / 256;  // 8 (D = 128) or 4 (D = 64)
+  const uint4* src = v + (bh * N + static_cast<long long>(kt) * 128) * VPR;
+  const int rows = N - kt * 128 < 128 ? N - kt * 128 : 128;
+  uint4 val[kPerThread];
+#pragma unroll
+  for (int u = 0; u < kPerThread; ++u) {
+    const int i = threadIdx.x + 256 * u;
+    val[u] = (i / VPR < rows) ? ld_stream(src + i) : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int u = 0; u < kPerThread; ++u) reinterpret_cast<uint4*>(tile)[threadIdx.x + 256 * u] = val[u];
+}
 
 // V [B,H,N,D] bf16 -> V^T codes [B,H,D,Npad/2] + E8M0 atoms.  One CTA per
 // (128-key tile, b*H+h).  The tile is staged in shared memory row-major;
@@ -147,40 +202,39 @@ __global__ void __launch_bounds__(256) mxfp4_v_kernel(const uint4* __restrict__ 
   const long long bh = blockIdx.y;
   const int ntiles = gridDim.x;
   const int npad_half = ntiles * 64;  // bytes per V^T row
-  constexpr int VPR = D / 8;          // 16-byte vectors per token row
-  for (int i = threadIdx.x; i < 128 * VPR; i += 256) {
-    const int r = i / VPR, cv = i % VPR;
-    const int n = kt * 128 + r;
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (n < N) val = ld_stream(v + ((bh * N + n) * VPR + cv));
-    *reinterpret_cast<uint4*>(&tile[r * D + cv * 8]) = val;
-  }
+  stage_v_tile<D>(v, tile, kt, bh, N);
   if (threadIdx.x < 128) atom[threadIdx.x] = 0u;
   __syncthreads();
-  for (int pidx = threadIdx.x; pidx < 4 * D; pidx += 256) {
-    const int d = pidx % D, kb = pidx / D;
-    uint32_t h[32];
-    uint32_t m = 0;
+  // a thread takes the channel pair (d, d+1) of one 32-key block: one 32-bit
+  // shared read per key, consecutive lanes on consecutive words
+  for (int pidx = threadIdx.x; pidx < 2 * D; pidx += 256) {
+    const int d0 = 2 * (pidx % (D / 2)), kb = pidx / (D / 2);
+    uint32_t w2[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      h[i] = tile[(kb * 32 + i) * D + d];
-      m = max(m, h[i] & 0x7FFFu);
+    for (int i = 0; i < 32; ++i) w2[i] = *reinterpret_cast<const uint32_t*>(&tile[(kb * 32 + i) * D + d0]);
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int d = d0 + c;
+      uint32_t m = 0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) m = max(m, (c ? (w2[i] >> 16) : w2[i]) & 0x7FFFu);
+      // e = smallest integer >= -127 with amax <= 6 * 2^e, from the bits of amax
+      const uint32_t ebits = m >> 7, frac = m & 0x7Fu;  // bf16: 8 exponent, 7 mantissa bits
+      int e = -127;
+      if (ebits != 0) e = max(-127, static_cast<int>(ebits) - 127 - (frac <= 0x40u ? 2 : 1));
+      const float inv_scale = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, e <= 126
+      float y[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        y[i] = __fmul_rn(__uint_as_float(c ? (w2[i] & 0xFFFF0000u) : (w2[i] << 16)), inv_scale);
+      uint4 out;
+      out.x = cvt_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
+      out.y = cvt_e2m1x8(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]);
+      out.z = cvt_e2m1x8(y[16], y[17], y[18], y[19], y[20], y[21], y[22], y[23]);
+      out.w = cvt_e2m1x8(y[24], y[25], y[26], y[27], y[28], y[29], y[30], y[31]);
+      __stcs(reinterpret_cast<uint4*>(payload_t + (bh * D + d) * npad_half + kt * 64 + kb * 16), out);
+      reinterpret_cast<uint8_t*>(atom)[(d & 31) * 16 + (d >> 5) * 4 + kb] = static_cast<uint8_t>(e + 127);
     }
-    // e = smallest integer >= -127 with amax <= 6 * 2^e, from the bits of amax
-    const uint32_t ebits = m >> 7, frac = m & 0x7Fu;  // bf16: 8 exponent, 7 mantissa bits
-    int e = -127;
-    if (ebits != 0) e = max(-127, static_cast<int>(ebits) - 127 - (frac <= 0x40u ? 2 : 1));
-    const float inv_scale = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, e <= 126
-    float y[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) y[i] = __fmul_rn(__uint_as_float(h[i] << 16), inv_scale);
-    uint4 out;
-    out.x = cvt_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
-    out.y = cvt_e2m1x8(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]);
-    out.z = cvt_e2m1x8(y[16], y[17], y[18], y[19], y[20], y[21], y[22], y[23]);
-    out.w = cvt_e2m1x8(y[24], y[25], y[26], y[27], y[28], y[29], y[30], y[31]);
-    __stcs(reinterpret_cast<uint4*>(payload_t + (bh * D + d) * npad_half + kt * 64 + kb * 16), out);
-    reinterpret_cast<uint8_t*>(atom)[(d & 31) * 16 + (d >> 5) * 4 + kb] = static_cast<uint8_t>(e + 127);
   }
   __syncthreads();
   if (threadIdx.x < 32)
@@ -199,42 +253,38 @@ __global__ void __launch_bounds__(256) mxfp8_v_kernel(const uint4* __restrict__ 
   const long long bh = blockIdx.y;
   const int ntiles = gridDim.x;
   const int npad = ntiles * 128;  // bytes per V^T row
-  constexpr int VPR = D / 8;
-  for (int i = threadIdx.x; i < 128 * VPR; i += 256) {
-    const int r = i / VPR, cv = i % VPR;
-    const int n = kt * 128 + r;
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (n < N) val = ld_stream(v + ((bh * N + n) * VPR + cv));
-    *reinterpret_cast<uint4*>(&tile[r * D + cv * 8]) = val;
-  }
+  stage_v_tile<D>(v, tile, kt, bh, N);
   if (threadIdx.x < 128) atom[threadIdx.x] = 0u;
   __syncthreads();
-  for (int pidx = threadIdx.x; pidx < 4 * D; pidx += 256) {
-    const int d = pidx % D, kb = pidx / D;
-    uint32_t h[32];
-    uint32_t m = 0;
+  for (int pidx = threadIdx.x; pidx < 2 * D; pidx += 256) {  // channel pairs, as in mxfp4_v_kernel
+    const int d0 = 2 * (pidx % (D / 2)), kb = pidx / (D / 2);
+    uint32_t w2[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      h[i] = tile[(kb * 32 + i) * D + d];
-      m = max(m, h[i] & 0x7FFFu);
+    for (int i = 0; i < 32; ++i) w2[i] = *reinterpret_cast<const uint32_t*>(&tile[(kb * 32 + i) * D + d0]);
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int d = d0 + c;
+      uint32_t m = 0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) m = max(m, (c ? (w2[i] >> 16) : w2[i]) & 0x7FFFu);
+      // e = smallest integer >= -127 with amax <= 448 * 2^e (448 = 1.75 * 2^8),
+      // from the bits of amax
+      const uint32_t ebits = m >> 7, frac = m & 0x7Fu;
+      int e = -127;
+      if (ebits != 0) e = max(-127, static_cast<int>(ebits) - 127 - (frac <= 0x60u ? 8 : 7));
+      const float inv_scale = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, e <= 121
+      float y[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        y[i] = __fmul_rn(__uint_as_float(c ? (w2[i] & 0xFFFF0000u) : (w2[i] << 16)), inv_scale);
+      uint32_t wd[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) wd[i] = cvt_e4m3x4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
+      uint4* dst = reinterpret_cast<uint4*>(payload_t + (bh * D + d) * npad + kt * 128 + kb * 32);
+      __stcs(dst, make_uint4(wd[0], wd[1], wd[2], wd[3]));
+      __stcs(dst + 1, make_uint4(wd[4], wd[5], wd[6], wd[7]));
+      reinterpret_cast<uint8_t*>(atom)[(d & 31) * 16 + (d >> 5) * 4 + kb] = static_cast<uint8_t>(e + 127);
     }
-    // e = smallest integer >= -127 with amax <= 448 * 2^e (448 = 1.75 * 2^8),
-    // from the bits of amax
-    const uint32_t ebits = m >> 7, frac = m & 0x7Fu;
-    int e = -127;
-    if (ebits != 0) e = max(-127, static_cast<int>(ebits) - 127 - (frac <= 0x60u ? 8 : 7));
-    const float inv_scale = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, e <= 121
-    uint32_t wd[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      wd[i] = cvt_e4m3x4(__fmul_rn(__uint_as_float(h[4 * i] << 16), inv_scale),
-                         __fmul_rn(__uint_as_float(h[4 * i + 1] << 16), inv_scale),
-                         __fmul_rn(__uint_as_float(h[4 * i + 2] << 16), inv_scale),
-                         __fmul_rn(__uint_as_float(h[4 * i + 3] << 16), inv_scale));
-    uint4* dst = reinterpret_cast<uint4*>(payload_t + (bh * D + d) * npad + kt * 128 + kb * 32);
-    __stcs(dst, make_uint4(wd[0], wd[1], wd[2], wd[3]));
-    __stcs(dst + 1, make_uint4(wd[4], wd[5], wd[6], wd[7]));
-    reinterpret_cast<uint8_t*>(atom)[(d & 31) * 16 + (d >> 5) * 4 + kb] = static_cast<uint8_t>(e + 127);
   }
   __syncthreads();
   if (threadIdx.x < 32)
@@ -266,9 +316,9 @@ extern "C" int fp4attn_quant_qk_nvfp4(const void* x, uint8_t* payload, uint8_t* 
   cudaError_t e = cudaMemsetAsync(g, 0, sizeof(float), s);
   if (e == cudaSuccess && (N % 128) != 0) e = cudaMemsetAsync(sf, 0, nvfp4_sf_bytes(B, H, N, D), s);
   if (e != cudaSuccess) return FP4ATTN_ERR_CUDA;
-  amax_kernel<<<grid_for(nvec, 256 * 4), 256, 0, s>>>(static_cast<const uint4*>(x), nvec,
+  amax_kernel<<<grid_for(nvec, 256 * kAmaxUnroll), 256, 0, s>>>(static_cast<const uint4*>(x), nvec,
                                                       reinterpret_cast<unsigned int*>(g));
-  nvfp4_quant_kernel<<<grid_for(nblocks, 256), 256, 0, s>>>(static_cast<const uint4*>(x),
+  nvfp4_quant_kernel<<<grid_for(nblocks, 256 * kQuantUnroll), 256, 0, s>>>(static_cast<const uint4*>(x),
                                                              reinterpret_cast<uint2*>(payload), sf, g, N, D, nblocks);
   nvfp4_finalize_kernel<<<1, 1, 0, s>>>(g);
   return cuda_status(cudaGetLastError());
