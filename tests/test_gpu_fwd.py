@@ -102,3 +102,19 @@ def test_side_streams_and_preallocated_outputs():
     assert fa.device_status() == fa.FP4ATTN_OK
     assert torch.equal(o1, o_ref) and torch.equal(l1, lse_ref)
     assert torch.equal(o2, oc_ref) and torch.equal(l2, lsec_ref)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_most_heads(causal):
+    # B*H = 65535, the most heads one launch takes (one grid row per head);
+    # a ragged 17-row sequence per head, so every head ends in a partial tile
+    import torch
+
+    B, H, N, D = 3, 21845, 17, 64
+    q, k, v = wl.make_custom(B, H, N, D, seed=55, kind="normal", scale=1.5)
+    heads = [0, 1, H - 1, H, 2 * H + 7, B * H - 1]
+    sample = sample_rows(B, H, N, heads, N, seed=55)
+    run_and_check(q, k, v, 1.0 / math.sqrt(D), [(B - 1, H - 1, 0, N)], sample,
+                  "65535 heads causal=%d" % causal, causal=causal)
+    del q, k, v
+    torch.cuda.empty_cache()
