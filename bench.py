@@ -8,7 +8,7 @@ over ranks (each rank runs its own replica of the workload: weak scaling).
 
 Default workload: B=1, H=40, N=32768, D=128 (video-DiT shape, token RMS
 spread), the largest configuration and the one the throughput target is
-quoted on.  Its inputs (1 GB bf16, 0.6 GB quantized) exceed the 129 MB L2, so
+quoted on.  Its inputs (1 GB bf16, 0.28 GB quantized) exceed the 129 MB L2, so
 no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
