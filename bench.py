@@ -53,12 +53,12 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic of one forward launch, from an ncu capture (see profiles/), and
 # the hash of the kernel sources it was taken on; reported only while the
 # sources are unchanged.
-TRAFFIC_RECORD = {"sources_sha": "7c860c7f45c7b1ad", "shape": (1, 40, 32768, 128),
-                  "bytes_per_launch": 279551744 + 291830784,
+TRAFFIC_RECORD = {"sources_sha": "d5b21613875f953b", "shape": (1, 40, 32768, 128),
+                  "bytes_per_launch": 278843648 + 291851520,
                   "note": "dram__bytes_read.sum + dram__bytes_write.sum of one launch on the 40-head "
                           "N=32768 D=128 workload (profiles/fwd_directp_B1_H40_N32768_D128_traffic.md)"}
 TRAFFIC_RECORD_CAUSAL = {"sources_sha": TRAFFIC_RECORD["sources_sha"], "shape": TRAFFIC_RECORD["shape"],
-                         "bytes_per_launch": 278415872 + 293369600,
+                         "bytes_per_launch": 278112512 + 293324032,
                          "note": "the same capture of the causal forward "
                                  "(profiles/fwd_directp_B1_H40_N32768_D128_traffic.md)"}
 KERNEL_SOURCES = ["blackwell_nvfp4_quantize_gb300/csrc/fwd_directp.cu", "blackwell_nvfp4_quantize_gb300/csrc/ptx.cuh"]

@@ -190,39 +190,10 @@ __host__ __device__ constexpr uint32_t idesc_mxf8_block_scaled(uint32_t M, uint3
          (a_sf_id & 3u) << 29;
 }
 
+// tcgen05 issues for a converged warp: every lane evaluates the operands (so
+// they stay warp-uniform) and elect.sync inside the asm picks the one lane
+// that issues.
 // D[tmem] (+)= A[smem] x B[smem]^T with NVFP4 scales (16-element blocks, UE4M3).
-__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t sfa_tmem, uint32_t sfb_tmem, bool accumulate) {
-  asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %6, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n}\n"
-      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate ? 1 : 0)
-      : "memory");
-}
-// D[tmem] (+)= A[smem] x B[smem]^T with MXFP4 scales (32-element blocks, UE8M0).
-__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t sfa_tmem, uint32_t sfb_tmem, bool accumulate) {
-  asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %6, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n}\n"
-      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate ? 1 : 0)
-      : "memory");
-}
-// Arrive on bar once every tcgen05 operation issued so far by this thread completes.
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-// Copy one 512-byte scale-factor atom (32 rows x 16 bytes in shared memory)
-// into 4 TMEM columns, replicated into all four 32-lane quarters.
-__device__ __forceinline__ void tc_cp_sf_atom(uint32_t taddr, const void* src) {
-  const uint64_t d = smem_desc(smem_u32(src), 128, 128, 0);
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
-}
-
-// The same tcgen05 issues for a converged warp: every lane evaluates the
-// operands (so they stay warp-uniform) and elect.sync inside the asm picks the
-// one lane that issues.
 __device__ __forceinline__ void mma_nvf4_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                               uint32_t sfa_tmem, uint32_t sfb_tmem, bool accumulate) {
   asm volatile(
@@ -231,6 +202,7 @@ __device__ __forceinline__ void mma_nvf4_warp(uint32_t d_tmem, uint64_t adesc, u
       ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate ? 1 : 0)
       : "memory");
 }
+// The same with MXFP4 scales (32-element blocks, UE8M0).
 __device__ __forceinline__ void mma_mxf4_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                               uint32_t sfa_tmem, uint32_t sfb_tmem, bool accumulate) {
   asm volatile(
@@ -248,12 +220,16 @@ __device__ __forceinline__ void mma_mxf8_warp(uint32_t d_tmem, uint64_t adesc, u
       ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate ? 1 : 0)
       : "memory");
 }
+// Arrive on bar once every tcgen05 operation issued so far by this warp's
+// elected lane completes.
 __device__ __forceinline__ void tc_commit_warp(uint64_t* bar) {
   asm volatile(
       "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(smem_u32(bar))
       : "memory");
 }
+// Copy one 512-byte scale-factor atom (32 rows x 16 bytes in shared memory)
+// into 4 TMEM columns, replicated into all four 32-lane quarters.
 __device__ __forceinline__ void tc_cp_sf_atom_warp(uint32_t taddr, uint32_t src_saddr) {
   const uint64_t d = smem_desc(src_saddr, 128, 128, 0);
   asm volatile(
@@ -311,9 +287,6 @@ __device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
   uint32_t r;
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
   return __uint_as_float(r);
-}
-__device__ __forceinline__ void tmem_st1(uint32_t taddr, float v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(__float_as_uint(v)) : "memory");
 }
 
 // ---------------------------------------------------------------- packed fp32 arithmetic
