@@ -171,6 +171,57 @@ def _check_input(x: torch.Tensor, name: str):
         raise ValueError("%s must be a contiguous CUDA bf16 tensor [B,H,N,D]" % name)
 
 
+# The C ABI takes plain pointers and cannot see buffer sizes: everything a
+# kernel will read or write is checked here, before the call, so that a
+# mismatched buffer raises instead of being read or written past its end.
+
+def _check_buffer(t: torch.Tensor, name: str, dtype, numel: int, device):
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or t.numel() != numel or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous %s tensor of %d elements" % (name, dtype, numel))
+    if t.device != device:
+        raise ValueError("%s is on %s, the operands on %s" % (name, t.device, device))
+
+
+def _check_quantized(t, name: str, shape, kind):
+    """t is a kind (NVFP4Tensor / MXFP4Tensor / MXFP8Tensor) of the given
+    shape whose buffers hold exactly the bytes the library reads."""
+    if not isinstance(t, kind):
+        raise ValueError("%s must be a %s" % (name, kind.__name__))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    B, H, N, D = shape
+    if kind is NVFP4Tensor:
+        pb, sb = nvfp4_bytes(B, H, N, D)
+        dev = t.payload.device
+        _check_buffer(t.payload, name + ".payload", torch.uint8, pb, dev)
+        _check_buffer(t.g, name + ".g", torch.float32, 1, dev)
+    else:
+        pb, sb = (mxfp4_v_bytes if kind is MXFP4Tensor else mxfp8_v_bytes)(B, H, N, D)
+        dev = t.payload_t.device
+        _check_buffer(t.payload_t, name + ".payload_t", torch.uint8, pb, dev)
+    _check_buffer(t.sf, name + ".sf", torch.uint8, sb, dev)
+    return dev
+
+
+def _check_fwd_args(q, k, v, v_kind, o, lse):
+    """Operands of one shape on one device; O bf16 [B,H,N,D] and LSE fp32
+    [B,H,N] (when given) on that device."""
+    if not isinstance(q, NVFP4Tensor):
+        raise ValueError("q must be an NVFP4Tensor")
+    shape = tuple(q.shape)
+    dev = _check_quantized(q, "q", shape, NVFP4Tensor)
+    for t, name, kind in ((k, "k", NVFP4Tensor), (v, "v", v_kind)):
+        if _check_quantized(t, name, shape, kind) != dev:
+            raise ValueError("q, k and v must be on one device")
+    B, H, N, D = shape
+    if o is not None:
+        _check_buffer(o, "o", torch.bfloat16, B * H * N * D, dev)
+    if lse is not None:
+        _check_buffer(lse, "lse", torch.float32, B * H * N, dev)
+    if dev.type != "cuda":
+        raise ValueError("the operands must be CUDA tensors")
+
+
 def empty_nvfp4(shape, device) -> NVFP4Tensor:
     B, H, N, D = shape
     pb, sb = nvfp4_bytes(B, H, N, D)
@@ -200,6 +251,8 @@ def quant_qk_nvfp4(x: torch.Tensor, out: NVFP4Tensor | None = None, stream=None)
     _check_input(x, "x")
     B, H, N, D = x.shape
     out = out or empty_nvfp4(x.shape, x.device)
+    if _check_quantized(out, "out", x.shape, NVFP4Tensor) != x.device:
+        raise ValueError("out must be on the device of x")
     _check(lib().fp4attn_quant_qk_nvfp4(_ptr(x), _ptr(out.payload), _ptr(out.sf), _ptr(out.g),
                                         B, H, N, D, ctypes.c_void_p(_stream(stream))), "fp4attn_quant_qk_nvfp4")
     return out
@@ -210,6 +263,8 @@ def quant_v_mxfp4(v: torch.Tensor, out: MXFP4Tensor | None = None, stream=None) 
     _check_input(v, "v")
     B, H, N, D = v.shape
     out = out or empty_mxfp4(v.shape, v.device)
+    if _check_quantized(out, "out", v.shape, MXFP4Tensor) != v.device:
+        raise ValueError("out must be on the device of v")
     _check(lib().fp4attn_quant_v_mxfp4(_ptr(v), _ptr(out.payload_t), _ptr(out.sf), B, H, N, D,
                                        ctypes.c_void_p(_stream(stream))), "fp4attn_quant_v_mxfp4")
     return out
@@ -220,6 +275,8 @@ def quant_v_mxfp8(v: torch.Tensor, out: MXFP8Tensor | None = None, stream=None) 
     _check_input(v, "v")
     B, H, N, D = v.shape
     out = out or empty_mxfp8(v.shape, v.device)
+    if _check_quantized(out, "out", v.shape, MXFP8Tensor) != v.device:
+        raise ValueError("out must be on the device of v")
     _check(lib().fp4attn_quant_v_mxfp8(_ptr(v), _ptr(out.payload_t), _ptr(out.sf), B, H, N, D,
                                        ctypes.c_void_p(_stream(stream))), "fp4attn_quant_v_mxfp8")
     return out
@@ -229,6 +286,7 @@ def fwd_directp_fp8pv(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP8Tensor, softmax_sc
                       causal: bool = False, o: torch.Tensor | None = None, lse: torch.Tensor | None = None,
                       stream=None):
     """fp4attn_fwd_directp_fp8pv: Direct-P with E4M3 probability codes and MXFP8 V; (O, LSE)."""
+    _check_fwd_args(q, k, v, MXFP8Tensor, o, lse)
     B, H, N, D = q.shape
     dev = q.payload.device
     if softmax_scale is None:
@@ -243,6 +301,7 @@ def fwd_directp_fp8pv(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP8Tensor, softmax_sc
 
 
 def _fwd(name, q, k, v, softmax_scale, o, lse, stream):
+    _check_fwd_args(q, k, v, MXFP4Tensor, o, lse)
     B, H, N, D = q.shape
     dev = q.payload.device
     if softmax_scale is None:
@@ -276,6 +335,8 @@ def fwd_directp_causal_save(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, s
     quantized Q/K and the LSE are what a backward pass reconstructs P from."""
     for x, name in ((q, "q"), (k, "k"), (v, "v")):
         _check_input(x, name)
+    if not (q.shape == k.shape == v.shape and q.device == k.device == v.device):
+        raise ValueError("q, k and v must have one shape and one device")
     B, H, N, D = q.shape
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
@@ -284,6 +345,12 @@ def fwd_directp_causal_save(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, s
     v_quant = v_quant or empty_mxfp4(v.shape, v.device)
     o = o if o is not None else torch.empty((B, H, N, D), dtype=torch.bfloat16, device=q.device)
     lse = lse if lse is not None else torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    for t, name, kind in ((q_saved, "q_saved", NVFP4Tensor), (k_saved, "k_saved", NVFP4Tensor),
+                          (v_quant, "v_quant", MXFP4Tensor)):
+        if _check_quantized(t, name, q.shape, kind) != q.device:
+            raise ValueError("%s must be on the device of q" % name)
+    _check_buffer(o, "o", torch.bfloat16, B * H * N * D, q.device)
+    _check_buffer(lse, "lse", torch.float32, B * H * N, q.device)
     qc, kc, vc = q_saved._c(), k_saved._c(), v_quant._c()
     _check(lib().fp4attn_fwd_directp_causal_save(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(qc), ctypes.byref(kc),
                                                  ctypes.byref(vc), _ptr(o), _ptr(lse), B, H, N, D,
@@ -297,6 +364,7 @@ def fwd_directp_noalloc(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP4Tensor, o: torch
     """fp4attn_fwd_directp_noalloc: the same forward with no device allocation
     anywhere on its path; the caller provides O and LSE.  A bounded wait that
     gives up shows as NaN in every LSE entry instead of a status code."""
+    _check_fwd_args(q, k, v, MXFP4Tensor, o, lse)
     B, H, N, D = q.shape
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
@@ -320,6 +388,10 @@ def debug_dump_p(q: NVFP4Tensor, k: NVFP4Tensor, v, b: int, h: int, row0: int, n
     o = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     fp8 = isinstance(v, MXFP8Tensor)
+    _check_fwd_args(q, k, v, MXFP8Tensor if fp8 else MXFP4Tensor, None, None)
+    if not (0 <= b < B and 0 <= h < H and 0 <= row0 and nrows > 0 and row0 + nrows <= N):
+        raise ValueError("dump rows (b=%d, h=%d, rows %d..%d) outside [B=%d, H=%d, N=%d]"
+                         % (b, h, row0, row0 + nrows, B, H, N))
     codes = torch.zeros((nrows, npad if fp8 else npad // 2), dtype=torch.uint8, device=dev)
     kshift = torch.zeros((nrows, npad // 32), dtype=torch.int32, device=dev)
     o32 = torch.zeros((nrows, D), dtype=torch.float32, device=dev)
