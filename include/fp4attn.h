@@ -149,9 +149,13 @@ int fp4attn_quant_v_mxfp8(const void *v, uint8_t *payload_t, uint8_t *sf,
  * "What the paper found": E2M1 probability codes from log-softmax scores,
  * denominator from the same rounded probabilities, LSE).
  * q, k: quantized NVFP4 tensors; v: quantized MXFP4 V; o: bf16 [B,H,N,D];
- * lse: fp32 [B,H,N].  softmax_scale must be finite and > 0.  One kernel
- * launch on stream.  Returns FP4ATTN_ERR_TIMEOUT only from
- * fp4attn_device_status; a launch returns OK or an argument/CUDA error. */
+ * lse: fp32 [B,H,N].  softmax_scale must be finite and > 0.  Block shifts
+ * and reference maxima are 32-bit integers, so every scaled score
+ * c*S = softmax_scale*log2(e)*q.k must stay below 2^30 in magnitude (for
+ * D = 128, amax(q)*amax(k) below about 7e7); larger scores are outside the
+ * supported range.  One kernel launch on stream.  Returns
+ * FP4ATTN_ERR_TIMEOUT only from fp4attn_device_status; a launch returns OK
+ * or an argument/CUDA error. */
 int fp4attn_fwd_directp(const fp4attn_nvfp4_t *q, const fp4attn_nvfp4_t *k, const fp4attn_mxfp4_t *v,
                         void *o, float *lse, int B, int H, int N, int D, float softmax_scale,
                         void *stream);
