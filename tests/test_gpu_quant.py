@@ -69,3 +69,21 @@ def test_quantizer_hand_worked_block(golden_dir):
     sf = t.sf.cpu().numpy()
     assert [int(sf[kb % 4 + 512 * (kb // 4)]) for kb in range(8)] == gold["sf_by_block"]
     assert t.g.item() == gold["g"]
+
+
+def test_quantizers_bit_exact_wrapping_grid_with_partial_chunk():
+    # 7 heads of 100003 rows at D = 64: the amax pass has more 8 KB warp
+    # chunks than warps (they wrap round the grid) and a partial last chunk
+    # (424 vectors); the NVFP4 pass wraps its 128-block warp groups and ends
+    # in a partial one (84 blocks); the V pass ends in a partial key tile
+    q, k, v = wl.make_custom(1, 7, 100003, 64, seed=313, kind="normal", scale=2.0)
+    import blackwell_nvfp4_quantize_gb300 as fa
+
+    _check_nvfp4(q)
+    _check_mxfp4(v)
+    x = torch.zeros((1, 7, 100003, 64), dtype=torch.bfloat16)
+    x.view(-1)[-1] = 1000.0  # the tensor maximum sits in the amax pass's last partial chunk
+    t = fa.quant_qk_nvfp4(x.cuda())
+    assert np.float32(t.g.item()) == np.float32(1000.0) / np.float32(2688.0)
+    del q, k, v, x
+    torch.cuda.empty_cache()
