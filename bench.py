@@ -19,6 +19,17 @@ tests) on a bounded sample of the same workload; it is a reported baseline.
 --causal times the causal forward instead (query i sees keys 0..i); its
 FLOPs are counted over the unmasked (query, key) pairs, 4*D*N*(N+1)/2 per head.
 --fp8pv times the FP8 P/V variant (MXFP8 V, E4M3 probability codes).
+
+The roofline peak is measured on the same GPU before the timed region: a loop
+of the block-scaled tcgen05 products the forward issues (QK^T: E2M1 with
+16-element UE4M3 scales; PV: E2M1 with 32-element UE8M0 scales, or E4M3 for
+the FP8 P/V variant), one CTA per SM (fp4attn_debug_mma_peak).  The forward
+spends half its FLOPs in each product, so its peak is the FLOP-weighted
+harmonic combination of the two rates.  The default run also times the
+forward of the D=64 workload and the causal and FP8 P/V forwards on the
+default workload, reported in "variants" of the same JSON line.
+
+  python bench.py --mma-peak   prints the measured peaks and the clocks seen
 """
 from __future__ import annotations
 
@@ -42,11 +53,9 @@ def metric_name(args):
     m = METRIC_CAUSAL if args.causal else METRIC
     return m.replace("FP4 attn", "FP4-QK/FP8-PV attn") if args.fp8pv else m
 UNIT = "TFLOP/s"
-# Dense FP4 : dense BF16 tensor throughput on GB300, nominal 13.5 : 2.25 PFLOP/s.
+# Context only (the roofline uses the measured block-scaled rates): nominal
+# dense FP4 : BF16 = 13.5 : 2.25 PFLOP/s, FP8 : BF16 = 4.5 : 2.25.
 FP4_OVER_BF16 = 13.5 / 2.25
-# FP8 P/V variant: QK^T (half the FLOPs) on FP4 operands, PV (the other half)
-# on FP8 operands at 4.5 : 2.25 of the BF16 rate -- the two halves take time in
-# sequence, so the combined peak is their harmonic combination.
 FP8PV_OVER_BF16 = 1.0 / (0.5 / FP4_OVER_BF16 + 0.5 / (4.5 / 2.25))
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -56,11 +65,10 @@ FALLBACK_BF16_TFLOPS = 1900.0
 TRAFFIC_RECORD = {"sources_sha": "d5b21613875f953b", "shape": (1, 40, 32768, 128),
                   "bytes_per_launch": 278843648 + 291851520,
                   "note": "dram__bytes_read.sum + dram__bytes_write.sum of one launch on the 40-head "
-                          "N=32768 D=128 workload (profiles/fwd_directp_B1_H40_N32768_D128_traffic.md)"}
+                          "N=32768 D=128 workload (ncu capture of the same kernel sources)"}
 TRAFFIC_RECORD_CAUSAL = {"sources_sha": TRAFFIC_RECORD["sources_sha"], "shape": TRAFFIC_RECORD["shape"],
                          "bytes_per_launch": 278112512 + 293324032,
-                         "note": "the same capture of the causal forward "
-                                 "(profiles/fwd_directp_B1_H40_N32768_D128_traffic.md)"}
+                         "note": "the same capture of the causal forward"}
 KERNEL_SOURCES = ["blackwell_nvfp4_quantize_gb300/csrc/fwd_directp.cu", "blackwell_nvfp4_quantize_gb300/csrc/ptx.cuh"]
 
 
@@ -135,6 +143,27 @@ class ClockSampler:
         loaded = [s for s in sm if smax and s > 0.5 * smax] or sm
         return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": smax,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measure_mma_peaks(iters=1 << 20, launches=3, rounds=3):
+    """Dense TFLOP/s of the block-scaled products the forward issues, best of
+    `rounds` timings of `launches` launches each (CUDA events)."""
+    import blackwell_nvfp4_quantize_gb300 as fa
+
+    out = {}
+    for kind in ("nvf4", "mxf4", "mxf8"):
+        fa.debug_mma_peak(kind, iters=1 << 14, launches=1)  # warm-up
+        out[kind] = max(fa.debug_mma_peak(kind, iters=iters, launches=launches) for _ in range(rounds))
+    if fa.device_status() != fa.FP4ATTN_OK:
+        raise RuntimeError("a bounded wait timed out in the MMA peak loop")
+    return out
+
+
+def forward_peak(peaks, fp8pv):
+    """The forward spends half of its FLOPs in QK^T and half in PV, one after
+    the other: its peak is the harmonic combination of the two rates."""
+    pv = peaks["mxf8"] if fp8pv else peaks["mxf4"]
+    return 1.0 / (0.5 / peaks["nvf4"] + 0.5 / pv)
 
 
 def attn_flops(rows, N, D, causal):
@@ -253,6 +282,76 @@ def run_reference(args, w):
     return 0
 
 
+def time_variant(w, causal, fp8pv, mma_peaks, dev, local, steps=10, warmup=3):
+    """Forward-only timing of one more configuration (CUDA events around each
+    launch, inputs resident in HBM, no flush: every variant's inputs exceed
+    the L2), with its own roofline and clocks."""
+    import torch
+
+    import blackwell_nvfp4_quantize_gb300 as fa
+    from blackwell_nvfp4_quantize_gb300 import workloads as wl
+
+    B, H, N, D = w.shape
+    stream = torch.cuda.current_stream()
+    q, k, v = (t.to(dev) for t in wl.make_inputs(w))
+    qq, kq = fa.quant_qk_nvfp4(q, stream=stream), fa.quant_qk_nvfp4(k, stream=stream)
+    vq = fa.quant_v_mxfp8(v, stream=stream) if fp8pv else fa.quant_v_mxfp4(v, stream=stream)
+    o = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    del q, k, v
+
+    def fwd():
+        if fp8pv:
+            fa.fwd_directp_fp8pv(qq, kq, vq, w.softmax_scale, causal=causal, o=o, lse=lse, stream=stream)
+        else:
+            (fa.fwd_directp_causal if causal else fa.fwd_directp)(qq, kq, vq, w.softmax_scale, o=o, lse=lse,
+                                                                 stream=stream)
+
+    for _ in range(warmup):
+        fwd()
+    torch.cuda.synchronize()
+    times = []
+    with ClockSampler(local) as clocks:
+        for _ in range(steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fwd()
+            e1.record(stream)
+            times.append((e0, e1))
+        torch.cuda.synchronize()
+    if fa.device_status() != fa.FP4ATTN_OK:
+        raise RuntimeError("device-side wait timed out in a variant")
+    ms = sum(a.elapsed_time(b) for a, b in times) / steps
+    flops = B * H * attn_flops(range(N), N, D, causal)
+    achieved = flops / (ms * 1e-3) / 1e12
+    peak = forward_peak(mma_peaks, fp8pv)
+    del qq, kq, vq, o, lse
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "B": B, "H": H, "N": N, "D": D, "mask": "causal" if causal else "none",
+            "pv": "fp8" if fp8pv else "fp4", "steps": steps, "warmup": warmup, "fwd_ms": ms,
+            "metric": "forward TFLOP/s (%s)" % ("4*D per unmasked (query, key) pair" if causal else "4BHN^2D/t"),
+            "value": achieved,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "peak_source": "measured block-scaled MMA loop, FLOP-weighted (see the main line)"},
+            "clocks": clocks.summary()}
+
+
+def run_mma_peak(args):
+    """--mma-peak: the block-scaled tensor rates of this GPU and the clocks they ran at."""
+    import torch
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    with ClockSampler(dev.index) as clocks:
+        peaks = measure_mma_peaks(iters=1 << 21, launches=5, rounds=5)
+    line = {"mma_peak_tflops": peaks, "forward_peak_fp4": forward_peak(peaks, False),
+            "forward_peak_fp8pv": forward_peak(peaks, True), "clocks": clocks.summary(),
+            "shape": "M=128, N=128, K=128 per round (two K=64 E2M1 or four K=32 E4M3 products), one CTA per SM"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_ours(args, w):
     import torch
 
@@ -302,6 +401,10 @@ def run_ours(args, w):
         else:
             fwd(qq, kq, vq, w.softmax_scale, o=o, lse=lse, stream=stream)
 
+    # roofline denominator: the block-scaled tensor rates of this GPU, measured
+    # now (about half a second), with the clocks they ran at
+    with ClockSampler(local) as peak_clocks:
+        mma_peaks = measure_mma_peaks()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -405,7 +508,8 @@ def run_ours(args, w):
     achieved = flops / (fwd_avg * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
     ratio = FP8PV_OVER_BF16 if args.fp8pv else FP4_OVER_BF16
-    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS)) * ratio
+    peak_nominal = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS)) * ratio
+    peak = forward_peak(mma_peaks, args.fp8pv)
     record = TRAFFIC_RECORD_CAUSAL if args.causal else TRAFFIC_RECORD
     traffic = (record["bytes_per_launch"]
                if (record["sources_sha"] == sources_sha() and not args.fp8pv and w.shape == record["shape"])
@@ -427,8 +531,14 @@ def run_ours(args, w):
         "fwd_frac_of_fp4_peak": achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": ("%s bf16 dense x %.1f (nominal %s dense ratio), burst"
-                                     % (peak_src, ratio, "FP4-QK/FP8-PV:BF16" if args.fp8pv else "FP4:BF16")),
+                     "peak_source": ("measured block-scaled tcgen05 MMA loop on this GPU (M=N=128, one CTA per "
+                                     "SM): QK^T kind::mxf4nvf4 %.0f, PV kind::%s %.0f TFLOP/s, FLOP-weighted "
+                                     "harmonic combination; burst"
+                                     % (mma_peaks["nvf4"], "mxf8f6f4" if args.fp8pv else "mxf4",
+                                        mma_peaks["mxf8" if args.fp8pv else "mxf4"])),
+                     "peak_clocks": peak_clocks.summary(),
+                     "frac_of_nominal_bf16_ratio": achieved / peak_nominal,
+                     "nominal_bf16_ratio_peak": peak_nominal,
                      "kernel": "fwd_directp_kernel<%d, causal=%s, fp8pv=%s>"
                                % (D, str(bool(args.causal)).lower(), str(bool(args.fp8pv)).lower())},
         "e2e": {"value": whole_job_tflops(world, flops, e2e_ms), "unit": UNIT,
@@ -438,6 +548,13 @@ def run_ours(args, w):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }
+    if rank == 0 and world == 1 and not args.no_variants and args.workload == 4 and not args.causal \
+            and not args.fp8pv:
+        del q, k, v, qq, kq, vq, o, lse, ins, outs, flush
+        torch.cuda.empty_cache()
+        line["variants"] = [time_variant(wl.WORKLOADS[5], False, False, mma_peaks, dev, local),
+                            time_variant(w, True, False, mma_peaks, dev, local),
+                            time_variant(w, False, True, mma_peaks, dev, local)]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, q_h, k_h, v_h, causal=args.causal, fp8pv=args.fp8pv)
     if rank == 0:
@@ -457,12 +574,17 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--causal", action="store_true", help="time the causal forward (query i sees keys 0..i)")
     ap.add_argument("--fp8pv", action="store_true", help="time the FP8 P/V variant (MXFP8 V, E4M3 codes)")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the D=64, causal and FP8 P/V forward timings of the default run")
+    ap.add_argument("--mma-peak", action="store_true", help="print the measured block-scaled tensor rates and exit")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     from blackwell_nvfp4_quantize_gb300 import workloads as wl
 
     w = wl.WORKLOADS[args.workload]
+    if args.mma_peak:
+        return run_mma_peak(args)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

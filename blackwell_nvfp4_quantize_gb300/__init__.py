@@ -83,7 +83,8 @@ def lib():
                                              ctypes.POINTER(_MXFP4), vp, vp, i, i, i, i, f, i, i, i, i, i, vp, vp,
                                              vp, vp]
     L.fp4attn_debug_wait_timeout.argtypes = [i, vp]
-    for name in ("fp4attn_debug_wait_timeout", "fp4attn_mxfp8_v_bytes", "fp4attn_quant_v_mxfp8", "fp4attn_fwd_directp_fp8pv",
+    L.fp4attn_debug_mma_peak.argtypes = [i, i, vp]
+    for name in ("fp4attn_debug_wait_timeout", "fp4attn_debug_mma_peak", "fp4attn_mxfp8_v_bytes", "fp4attn_quant_v_mxfp8", "fp4attn_fwd_directp_fp8pv",
                  "fp4attn_debug_dump_p_fp8pv", "fp4attn_fwd_directp_causal", "fp4attn_debug_dump_p_causal", "fp4attn_fwd_directp_causal_save",
                  "fp4attn_fwd_directp_noalloc", "fp4attn_debug_cvt_transitions", "fp4attn_nvfp4_bytes", "fp4attn_mxfp4_v_bytes", "fp4attn_quant_qk_nvfp4",
                  "fp4attn_quant_v_mxfp4", "fp4attn_fwd_directp", "fp4attn_debug_dump_p",
@@ -418,6 +419,28 @@ def debug_wait_timeout(limit_us: int, stream=None) -> None:
     """fp4attn_debug_wait_timeout: a bounded wait that nothing completes gives up after limit_us."""
     _check(lib().fp4attn_debug_wait_timeout(int(limit_us), ctypes.c_void_p(_stream(stream))),
            "fp4attn_debug_wait_timeout")
+
+
+MMA_PEAK_KINDS = {"nvf4": 0, "mxf4": 1, "mxf8": 2}
+
+
+def debug_mma_peak(kind: str, iters: int = 1 << 20, launches: int = 3, stream=None):
+    """fp4attn_debug_mma_peak: dense TFLOP/s of the block-scaled product `kind`
+    ("nvf4": QK^T form, "mxf4": PV form, "mxf8": FP8 PV form), timed with CUDA
+    events over `launches` launches after one warm-up launch."""
+    st = torch.cuda.current_stream() if stream is None else stream
+    code = MMA_PEAK_KINDS[kind]
+    _check(lib().fp4attn_debug_mma_peak(code, int(iters), ctypes.c_void_p(_stream(st))), "fp4attn_debug_mma_peak")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(launches):
+        _check(lib().fp4attn_debug_mma_peak(code, int(iters), ctypes.c_void_p(_stream(st))),
+               "fp4attn_debug_mma_peak")
+    e1.record(st)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / launches
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return sms * float(iters) * 2.0 * 128 ** 3 / (ms * 1e-3) / 1e12
 
 
 def debug_cvt_transitions(fmt: int, lo: int, hi: int, capacity: int = 4096, stream=None):

@@ -55,10 +55,103 @@ __global__ void __launch_bounds__(32) wait_timeout_kernel(uint64_t limit_ns, Dev
   mbar_wait(&bar, 0, &abort_flag, status, 90, limit_ns);
 }
 
+// Dense tensor-core throughput of the block-scaled products the forward
+// issues, for the roofline: one CTA per SM, one elected thread issues `iters`
+// rounds of M = 128, N = 128 products from shared-memory operands into one
+// TMEM accumulator.  kind 0: kind::mxf4nvf4 (E2M1, 16-element UE4M3 scales,
+// two K = 64 products per round, the QK^T form); kind 1: kind::mxf4 (E2M1,
+// 32-element UE8M0 scales, two K = 64 products, the PV form); kind 2:
+// kind::mxf8f6f4 (E4M3, one UE8M0 scale per 32 elements, four K = 32
+// products, the FP8 PV form).  Every round is 2*128*128*128 FLOP.  Operands
+// are E2M1 / E4M3 ones with unit scales.
+constexpr int kPeakThreads = 128;
+// 35 KB used; the request is padded so that one CTA holds each SM
+constexpr int kPeakSmem = 120 * 1024;
+
+__global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int kind, int iters, DeviceStatus* status) {
+  extern __shared__ uint8_t raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* a = smem;              // 128 rows x 64 B (E2M1) or 128 B (E4M3)
+  uint8_t* b = smem + 16384;      // the same
+  uint8_t* sf = smem + 32768;     // A scale atoms (2), B scale atoms (2)
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 32768 + 4 * 512);
+  uint32_t* slot = reinterpret_cast<uint32_t*>(smem + 32768 + 4 * 512 + 8);
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x >> 5;
+  const uint32_t one4 = (kind == 2) ? 0x38383838u : 0x22222222u;    // E4M3 1.0 / two E2M1 1.0
+  const uint32_t unit4 = (kind == 0) ? 0x38383838u : 0x7F7F7F7Fu;   // UE4M3 1.0 / UE8M0 1.0
+  for (int i = threadIdx.x; i < 32768 / 16; i += kPeakThreads)
+    reinterpret_cast<uint4*>(smem)[i] = make_uint4(one4, one4, one4, one4);
+  for (int i = threadIdx.x; i < 4 * 512 / 16; i += kPeakThreads)
+    reinterpret_cast<uint4*>(sf)[i] = make_uint4(unit4, unit4, unit4, unit4);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  fence_proxy_async_smem();
+  if (warp == 0) {
+    tmem_alloc(slot, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot;
+  if (warp == 0) {
+    const uint32_t d = tmem, sfa = tmem + 128, sfb = tmem + 136;
+    for (int i = 0; i < 2; ++i) {
+      tc_cp_sf_atom_warp(sfa + 4 * i, smem_u32(sf + 512 * i));
+      tc_cp_sf_atom_warp(sfb + 4 * i, smem_u32(sf + 1024 + 512 * i));
+    }
+    if (kind == 2) {
+      const uint64_t ad = smem_desc(smem_u32(a), 16, 1024, 2), bd = smem_desc(smem_u32(b), 16, 1024, 2);
+      for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_mxf8_warp(d, ad + 2 * k, bd + 2 * k, idesc_mxf8_block_scaled(128, 128, k, k), sfa, sfb, it > 0 || k > 0);
+      }
+    } else if (kind == 1) {
+      const uint64_t ad = smem_desc(smem_u32(a), 16, 512, 4), bd = smem_desc(smem_u32(b), 16, 512, 4);
+      constexpr uint32_t i0 = idesc_fp4_block_scaled(128, 128, 1, 0, 0), i1 = idesc_fp4_block_scaled(128, 128, 1, 2, 2);
+      for (int it = 0; it < iters; ++it) {
+        mma_mxf4_warp(d, ad, bd, i0, sfa, sfb, it > 0);
+        mma_mxf4_warp(d, ad + 2, bd + 2, i1, sfa, sfb, true);
+      }
+    } else {
+      const uint64_t ad = smem_desc(smem_u32(a), 16, 512, 4), bd = smem_desc(smem_u32(b), 16, 512, 4);
+      constexpr uint32_t i0 = idesc_fp4_block_scaled(128, 128, 0, 0, 0);
+      for (int it = 0; it < iters; ++it) {
+        mma_nvf4_warp(d, ad, bd, i0, sfa, sfb, it > 0);
+        mma_nvf4_warp(d, ad + 2, bd + 2, i0, sfa + 4, sfb + 4, true);
+      }
+    }
+    tc_commit_warp(bar);
+    mbar_wait_drain(bar, 0, &abort_flag, status, 91);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) {
+    __syncwarp();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
 }  // namespace
 }  // namespace fp4attn
 
 using namespace fp4attn;
+
+extern "C" int fp4attn_debug_mma_peak(int kind, int iters, void* stream) {
+  if (kind < 0 || kind > 2 || iters <= 0 || iters > (1 << 26)) return FP4ATTN_ERR_INVALID_ARG;
+  DeviceStatus* status = device_status_ptr();
+  if (!status) return FP4ATTN_ERR_CUDA;
+  if (cudaFuncSetAttribute(mma_peak_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPeakSmem) != cudaSuccess)
+    return FP4ATTN_ERR_CUDA;
+  mma_peak_kernel<<<sm_count(), kPeakThreads, kPeakSmem, static_cast<cudaStream_t>(stream)>>>(kind, iters, status);
+  return cuda_status(cudaGetLastError());
+}
 
 extern "C" int fp4attn_debug_wait_timeout(int limit_us, void* stream) {
   if (limit_us <= 0 || limit_us > 1000000) return FP4ATTN_ERR_INVALID_ARG;

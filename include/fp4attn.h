@@ -271,6 +271,19 @@ int fp4attn_debug_cvt_transitions(int format, uint32_t lo, uint32_t hi, uint32_t
  * FP4ATTN_ERR_TIMEOUT once) and the kernel returns normally. */
 int fp4attn_debug_wait_timeout(int limit_us, void *stream);
 
+/* Measurement support (no counterpart on the pages): the dense tensor-core
+ * rate of the block-scaled products the forward issues, the denominator of
+ * its roofline.  Launches one CTA per SM; one thread per CTA issues `iters`
+ * rounds of M = 128, N = 128, K = 128 products (2*128^3 FLOP per round) from
+ * shared-memory operands into a TMEM accumulator:
+ *   kind 0  kind::mxf4nvf4, E2M1 x E2M1, 16-element UE4M3 scales (QK^T form)
+ *   kind 1  kind::mxf4,     E2M1 x E2M1, 32-element UE8M0 scales (PV form)
+ *   kind 2  kind::mxf8f6f4, E4M3 x E4M3, 32-element UE8M0 scales (FP8 PV form)
+ * The caller times the launch on `stream` (FLOP = SMs * iters * 2 * 128^3).
+ * Errors: FP4ATTN_ERR_INVALID_ARG for kind outside 0..2 or iters outside
+ * 1..2^26; a wait that gives up shows in fp4attn_device_status. */
+int fp4attn_debug_mma_peak(int kind, int iters, void *stream);
+
 /* Reads and clears the status word the kernels of this library set when a
  * bounded device-side wait gives up (they then stop early and leave their
  * outputs incomplete).  Synchronises the given stream first.  Returns

@@ -134,3 +134,12 @@ def test_fp8pv_argument_errors_without_gpu(L):
                                        ctypes.c_float(0.1), 1, n) == fa.FP4ATTN_ERR_INVALID_ARG
     assert L.fp4attn_debug_dump_p_fp8pv(*args, ctypes.c_float(0.1), 0, 0, 0, 100, 64, good, good, good, n) == \
         fa.FP4ATTN_ERR_INVALID_ARG  # rows beyond N
+
+
+def test_mma_peak_argument_errors(L):
+    import blackwell_nvfp4_quantize_gb300 as fa
+
+    assert L.fp4attn_debug_mma_peak(3, 16, None) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert L.fp4attn_debug_mma_peak(-1, 16, None) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert L.fp4attn_debug_mma_peak(0, 0, None) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert L.fp4attn_debug_mma_peak(1, (1 << 26) + 1, None) == fa.FP4ATTN_ERR_INVALID_ARG
