@@ -74,6 +74,12 @@ def _load():
                                      c_int, c_int, c_int, c_int, ctypes.c_float, c_int, c_int, i64p, c_int,
                                      f64p, f64p, u8p, i32p, i32p, c_int]
     lib.orc_directp_rows.restype = None
+    lib.orc_directp_rows_ex.argtypes = [u8p, u8p, ctypes.c_float, u8p, u8p, ctypes.c_float, u8p, u8p,
+                                        c_int, c_int, c_int, c_int, ctypes.c_float, c_int, c_int, c_int, i64p, c_int,
+                                        f64p, f64p, u8p, i32p, i32p, c_int]
+    lib.orc_directp_rows_ex.restype = None
+    lib.orc_directp_map_row_f64.argtypes = [f64p, c_int, ctypes.c_double, c_int, u8p, i32p, i32p, f64p]
+    lib.orc_directp_map_row_f64.restype = None
     lib.orc_directp_map_row.argtypes = [f32p, c_int, ctypes.c_float, c_int, u8p, i32p, i32p, f64p]
     lib.orc_directp_map_row.restype = None
     lib.orc_exact_rows.argtypes = [u16p, u16p, u16p, c_int, c_int, c_int, c_int, ctypes.c_double, c_int,
@@ -173,13 +179,14 @@ PV_MXFP4, PV_MXFP8 = 0, 1
 # ---- attention -----------------------------------------------------------
 
 def directp_rows(q, k, v, shape, softmax_scale, rows, threads=None, want_codes=False, causal=False,
-                 pv_fmt=PV_MXFP4):
+                 pv_fmt=PV_MXFP4, f64_decisions=False):
     """Direct-P forward for selected rows.
 
     q, k: (payload, sf, g) as returned by quant_nvfp4; v: (payload_t, sf) from
     quant_mxfp4_v (pv_fmt PV_MXFP4: E2M1 P and V) or quant_mxfp8_v (PV_MXFP8:
     E4M3 P and V).  rows: int64 flat row ids (b*H + h)*N + i.  causal: row i
-    sees keys 0..i.
+    sees keys 0..i.  f64_decisions: take the mapping's decisions in fp64 (S,
+    c, X and X - K_b not rounded to fp32) instead of the kernel's fp32.
     Returns dict with o [R,D] f64, lse [R] f64 and, when want_codes, codes
     [R,Npad] u8 (one code per byte), kshift [R,Npad/32] i32, m [R] i32.
     """
@@ -202,11 +209,12 @@ def directp_rows(q, k, v, shape, softmax_scale, rows, threads=None, want_codes=F
     vp, vsf = [np.ascontiguousarray(t) for t in v]
     null_u8 = ctypes.POINTER(ctypes.c_uint8)()
     null_i32 = ctypes.POINTER(ctypes.c_int32)()
-    lib.orc_directp_rows(
+    lib.orc_directp_rows_ex(
         _ptr(qp, ctypes.c_uint8), _ptr(qsf, ctypes.c_uint8), float(gq),
         _ptr(kp, ctypes.c_uint8), _ptr(ksf, ctypes.c_uint8), float(gk),
         _ptr(vp, ctypes.c_uint8), _ptr(vsf, ctypes.c_uint8),
-        B, H, N, D, float(softmax_scale), int(bool(causal)), int(pv_fmt), _ptr(rows, ctypes.c_int64), R,
+        B, H, N, D, float(softmax_scale), int(bool(causal)), int(pv_fmt), int(bool(f64_decisions)),
+        _ptr(rows, ctypes.c_int64), R,
         _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
         _ptr(codes, ctypes.c_uint8) if want_codes else null_u8,
         _ptr(kshift, ctypes.c_int32) if want_codes else null_i32,
@@ -226,6 +234,20 @@ def directp_map_row(s: np.ndarray, c: float, pv_fmt=PV_MXFP4):
     l = ctypes.c_double(0.0)
     lib.orc_directp_map_row(_ptr(s, ctypes.c_float), n, float(c), int(pv_fmt), _ptr(codes, ctypes.c_uint8),
                             _ptr(ks, ctypes.c_int32), ctypes.byref(m), ctypes.byref(l))
+    return codes, ks, int(m.value), float(l.value)
+
+
+def directp_map_row_f64(s: np.ndarray, c: float, pv_fmt=PV_MXFP4):
+    """One row of fp64 scores mapped with fp64 decisions -> (codes, kshift, M, l)."""
+    lib = _load()
+    s = np.ascontiguousarray(s, dtype=np.float64)
+    n = s.shape[0]
+    codes = np.zeros((n,), dtype=np.uint8)
+    ks = np.zeros(((n + 31) // 32,), dtype=np.int32)
+    m = ctypes.c_int32(0)
+    l = ctypes.c_double(0.0)
+    lib.orc_directp_map_row_f64(_ptr(s, ctypes.c_double), n, float(c), int(pv_fmt), _ptr(codes, ctypes.c_uint8),
+                                _ptr(ks, ctypes.c_int32), ctypes.byref(m), ctypes.byref(l))
     return codes, ks, int(m.value), float(l.value)
 
 

@@ -372,6 +372,47 @@ void orc_directp_map_row(const float *s, int n, float c, int fmt,
     *l_out = l;
 }
 
+/* The same row mapping with every decision taken in fp64: X = c*S in fp64
+ * (S and c not rounded to fp32), K_b = ceil(X_b - log2 R) with the fp64
+ * log2 R, code = E2M1/E4M3 of the exact 2^(X - K_b).  This is the plainest
+ * reading of the mapping ("What the paper found": scores mapped directly to
+ * codes); orc_directp_map_row takes the same decisions in fp32, the
+ * precision the forward kernel computes in. */
+void orc_directp_map_row_f64(const double *s, int n, double c, int fmt,
+                             uint8_t *codes, int32_t *kshift, int32_t *m_out,
+                             double *l_out) {
+    const double log2_max = log2((fmt == ORC_PV_MXFP8) ? 448.0 : 6.0);
+    int nblk = (n + 31) / 32;
+    double xmax = -INFINITY;
+    for (int j = 0; j < n; j++) {
+        double x = c * s[j];
+        if (x > xmax) xmax = x;
+    }
+    int32_t M = (int32_t)ceil(xmax);
+    double l = 0.0;
+    for (int b = 0; b < nblk; b++) {
+        int j0 = b * 32, j1 = j0 + 32 < n ? j0 + 32 : n;
+        double xb = -INFINITY;
+        for (int j = j0; j < j1; j++) {
+            double x = c * s[j];
+            if (x > xb) xb = x;
+        }
+        int32_t K = (int32_t)ceil(xb - log2_max);
+        kshift[b] = K;
+        int e = K - M;
+        if (e < -127) e = -127;
+        double scale = ldexp(1.0, e);
+        for (int j = j0; j < j1; j++) {
+            double p = exp2(c * s[j] - (double)K);
+            uint8_t code = (fmt == ORC_PV_MXFP8) ? orc_e4m3_encode(p) : orc_e2m1_encode(p);
+            codes[j] = code;
+            l += ((fmt == ORC_PV_MXFP8) ? orc_e4m3_decode(code) : orc_e2m1_decode(code)) * scale;
+        }
+    }
+    *m_out = M;
+    *l_out = l;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Direct-P attention rows                                                  */
 /* ------------------------------------------------------------------------ */
@@ -386,6 +427,8 @@ typedef struct {
     int B, H, N, D;
     int causal; /* row i sees keys 0..i only */
     int pv_fmt; /* ORC_PV_MXFP4 or ORC_PV_MXFP8 */
+    int f64_decisions; /* map with orc_directp_map_row_f64 (fp64 S, c, X) */
+    double c64; /* the multiplier in fp64 */
     /* per-head decoded operands */
     long bh;
     double *khat; /* [N][D] */
@@ -432,6 +475,7 @@ static void attn_rows_chunk(void *p, long lo, long hi) {
     const int N = a->N, D = a->D, KB = D / 16, Npad = row_tiles(N) * 128;
     double *qhat = (double *)malloc(sizeof(double) * (size_t)D);
     float *s32 = (float *)malloc(sizeof(float) * (size_t)N);
+    double *s64 = (double *)malloc(sizeof(double) * (size_t)N);
     uint8_t *codes = (uint8_t *)malloc((size_t)Npad);
     int32_t *ks = (int32_t *)malloc(sizeof(int32_t) * (size_t)(Npad / 32));
     double *acc = (double *)malloc(sizeof(double) * (size_t)D);
@@ -452,12 +496,16 @@ static void attn_rows_chunk(void *p, long lo, long hi) {
             double s = 0.0;
             for (int d = 0; d < D; d++) s += qhat[d] * a->khat[(size_t)j * D + d];
             s32[j] = (float)s;
+            s64[j] = s;
         }
         memset(codes, 0, (size_t)Npad);
         memset(ks, 0, sizeof(int32_t) * (size_t)(Npad / 32));
         int32_t M;
         double l;
-        orc_directp_map_row(s32, nk, a->c, a->pv_fmt, codes, ks, &M, &l);
+        if (a->f64_decisions)
+            orc_directp_map_row_f64(s64, nk, a->c64, a->pv_fmt, codes, ks, &M, &l);
+        else
+            orc_directp_map_row(s32, nk, a->c, a->pv_fmt, codes, ks, &M, &l);
         for (int d = 0; d < D; d++) acc[d] = 0.0;
         for (int j = 0; j < nk; j++) {
             int e = ks[j / 32] - M;
@@ -475,6 +523,7 @@ static void attn_rows_chunk(void *p, long lo, long hi) {
     }
     free(qhat);
     free(s32);
+    free(s64);
     free(codes);
     free(ks);
     free(acc);
@@ -488,6 +537,18 @@ void orc_directp_rows(const uint8_t *q_payload, const uint8_t *q_sf, float g_q,
                       double *o, double *lse,
                       uint8_t *codes, int32_t *kshift, int32_t *mrow,
                       int nthreads) {
+    orc_directp_rows_ex(q_payload, q_sf, g_q, k_payload, k_sf, g_k, v_payload_t, v_sf, B, H, N, D,
+                        softmax_scale, causal, pv_fmt, 0, rows, nrows, o, lse, codes, kshift, mrow, nthreads);
+}
+
+void orc_directp_rows_ex(const uint8_t *q_payload, const uint8_t *q_sf, float g_q,
+                         const uint8_t *k_payload, const uint8_t *k_sf, float g_k,
+                         const uint8_t *v_payload_t, const uint8_t *v_sf,
+                         int B, int H, int N, int D, float softmax_scale, int causal, int pv_fmt,
+                         int f64_decisions, const int64_t *rows, int nrows,
+                         double *o, double *lse,
+                         uint8_t *codes, int32_t *kshift, int32_t *mrow,
+                         int nthreads) {
     attn_ctx a;
     memset(&a, 0, sizeof a);
     a.qp = q_payload;
@@ -504,8 +565,11 @@ void orc_directp_rows(const uint8_t *q_payload, const uint8_t *q_sf, float g_q,
     a.D = D;
     a.causal = causal;
     a.pv_fmt = pv_fmt;
-    /* the log2-domain score multiplier, rounded once to fp32 */
-    a.c = (float)((((double)softmax_scale * LOG2E) * (double)g_q) * (double)g_k);
+    /* the log2-domain score multiplier, rounded once to fp32 (and kept in
+     * fp64 for the fp64-decision reading) */
+    a.c64 = (((double)softmax_scale * LOG2E) * (double)g_q) * (double)g_k;
+    a.c = (float)a.c64;
+    a.f64_decisions = f64_decisions;
     a.rows = rows;
     a.o = o;
     a.lse = lse;

@@ -133,6 +133,28 @@ void orc_directp_rows(const uint8_t *q_payload, const uint8_t *q_sf, float g_q,
                       uint8_t *codes, int32_t *kshift, int32_t *mrow,
                       int nthreads);
 
+/* orc_directp_rows with a choice of the precision the mapping's decisions
+ * are taken in.  f64_decisions = 0: as above (S, c, X and t rounded to fp32,
+ * as the forward kernel computes them).  f64_decisions = 1: the plain fp64
+ * reading -- X = c*S with S and c in fp64, K_b = ceil(X_b - log2 R) and the
+ * code of the exact 2^(X - K_b) all in fp64 (orc_directp_map_row_f64).
+ * Pinned: the two readings differ only where fp32 rounding moves a value
+ * across a decision threshold (a code boundary of 2^t or an integer of
+ * X_b - log2 R), checked against the fp64 distance to that threshold. */
+void orc_directp_rows_ex(const uint8_t *q_payload, const uint8_t *q_sf, float g_q,
+                         const uint8_t *k_payload, const uint8_t *k_sf, float g_k,
+                         const uint8_t *v_payload_t, const uint8_t *v_sf,
+                         int B, int H, int N, int D, float softmax_scale, int causal, int pv_fmt,
+                         int f64_decisions, const int64_t *rows, int nrows,
+                         double *o, double *lse,
+                         uint8_t *codes, int32_t *kshift, int32_t *mrow,
+                         int nthreads);
+
+/* One row of fp64 scores mapped with fp64 decisions (see above). */
+void orc_directp_map_row_f64(const double *s, int n, double c, int fmt,
+                             uint8_t *codes, int32_t *kshift, int32_t *m_out,
+                             double *l_out);
+
 /* The same row pass on explicit scores: for one row of n fp32 scores S,
  * multiplier c and code format fmt, returns the codes (n bytes), K_b per
  * 32-key block, M and l (with p = dec(code)*2^e_b as above).  Used to pin the
