@@ -3,7 +3,10 @@ oracle's numpy form, run the forward and compare it with the oracle.
 
 Parity bar: probability codes agree on >= 99.9% of entries (ties may flip
 with fp32 accumulation order), block shifts likewise, O within max-abs 2e-2
-and LSE within 1e-3."""
+and LSE within 1e-3.  Codes and block shifts are compared with both readings
+of the oracle's decisions: in fp32 (the kernel's precision) and in fp64 (S,
+c, X and X - K_b unrounded, the plain reading of the method); both must agree
+on >= 99.9%."""
 import numpy as np
 import torch
 
@@ -27,11 +30,15 @@ def unpack_codes(packed: np.ndarray) -> np.ndarray:
 
 
 def sample_rows(B, H, N, heads, rows_per_head, seed):
-    """Flat row ids (b*H+h)*N+i: chosen heads, rows spread over [0, N) incl. both ends."""
+    """Flat row ids (b*H+h)*N+i: for each chosen head, rows 0 and N-1 and one
+    random row in each of rows_per_head equal strata of [0, N)."""
     rng = np.random.default_rng(seed)
+    n = min(N, rows_per_head)
+    edges = np.linspace(0, N, n + 1).astype(np.int64)
     out = []
     for bh in heads:
-        r = np.unique(np.concatenate([[0, N - 1], rng.choice(N, size=min(N, rows_per_head), replace=False)]))
+        r = [rng.integers(lo, hi) for lo, hi in zip(edges[:-1], edges[1:]) if hi > lo]
+        r = np.unique(np.concatenate([[0, N - 1], np.array(r, dtype=np.int64)]))
         out.extend(int(bh) * N + int(i) for i in r)
     return np.array(sorted(set(out)), dtype=np.int64)
 
@@ -45,10 +52,11 @@ def cosine(a, b):
 O_TOL = 2e-2
 LSE_TOL = 1e-3
 CODE_AGREE = 0.999
-# O is stored in bf16 (round to nearest even: relative error <= 2^-9).  The
-# 2e-2 absolute bound applies to O as computed (fp32, before that store, read
-# through the dump entry point); the stored bf16 O is checked against
-# 2e-2 plus its own rounding, and to be exactly the rounding of the fp32 value.
+# O is stored in bf16: an 8-bit significand, so round to nearest even has a
+# relative error up to 2^-8 (1 + 2^-8 rounds to 1.0).  The 2e-2 absolute bound
+# applies to O as computed (fp32, before that store, read through the dump
+# entry point); the stored bf16 O is checked against 2e-2 plus its own
+# rounding, and to be exactly the rounding of the fp32 value.
 BF16_REL = 2.0 ** -8
 
 
@@ -86,7 +94,7 @@ def run_and_check(q, k, v, scale, dump_slices, sample, label, causal=False, fp8p
     err_o16 = float(np.max(np.abs(o_np[sample] - ref["o"]) - BF16_REL * np.abs(ref["o"])))
     err_l = float(np.max(np.abs(lse_np[sample] - ref["lse"])))
     # codes, block shifts and fp32 O through the dump entry point (same kernel and launch shape)
-    agree = total = kagree = ktotal = 0
+    agree = total = kagree = ktotal = agree64 = kagree64 = 0
     err_o32 = 0.0
     for (b, h, row0, nrows) in dump_slices:
         o2, lse2, codes, kshift, o32 = fa.debug_dump_p(qq, kq, vq, b, h, row0, nrows, scale, causal=causal)
@@ -106,15 +114,23 @@ def run_and_check(q, k, v, scale, dump_slices, sample, label, causal=False, fp8p
         gk = kshift.cpu().numpy()[:, :nblk]
         kagree += int(np.sum(gk == r["kshift"][:, :nblk]))
         ktotal += gk.size
+        r64 = oracle.directp_rows(qn, kn, vn, (B, H, N, D), scale, rows, want_codes=True, causal=causal,
+                                  pv_fmt=pv_fmt, f64_decisions=True)
+        agree64 += int(np.sum(gc[:, :N] == r64["codes"][:, :N]))
+        kagree64 += int(np.sum(gk == r64["kshift"][:, :nblk]))
         assert np.all(gc[:, N:] == 0)
     frac = agree / max(total, 1)
     kfrac = kagree / max(ktotal, 1)
-    print("%s: max|dO32|=%.3g max|dO16|-bf16=%.3g max|dLSE|=%.3g codes agree %.6f kshift agree %.6f"
-          % (label, err_o32, err_o16, err_l, frac, kfrac))
+    frac64 = agree64 / max(total, 1)
+    kfrac64 = kagree64 / max(ktotal, 1)
+    print("%s: max|dO32|=%.3g max|dO16|-bf16=%.3g max|dLSE|=%.3g codes agree %.6f (fp64 reading %.6f) "
+          "kshift agree %.6f (fp64 reading %.6f)" % (label, err_o32, err_o16, err_l, frac, frac64, kfrac, kfrac64))
     assert err_o32 <= O_TOL, err_o32
     assert err_o16 <= O_TOL, err_o16
     assert err_l <= LSE_TOL, err_l
     if total:
         assert frac >= CODE_AGREE, frac
         assert kfrac >= CODE_AGREE, kfrac
+        assert frac64 >= CODE_AGREE, frac64
+        assert kfrac64 >= CODE_AGREE, kfrac64
     return o_np, lse_np

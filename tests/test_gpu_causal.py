@@ -30,12 +30,13 @@ def test_causal_workloads_sampled(idx):
     w = wl.WORKLOADS[idx]
     q, k, v = wl.make_inputs(w)
     B, H, N, D = w.shape
-    heads = sorted({0, B * H - 1, (B * H) // 2})
-    sample = sample_rows(B, H, N, heads, 48 if idx == 4 else 96, seed=100 + idx)
+    # every head, rows spread over the sequence (short early rows and full
+    # late rows alike); full slices at the first rows, the last rows and the
+    # middle of a middle head
+    sample = sample_rows(B, H, N, range(B * H), 16 if idx in (4, 5) else 48, seed=100 + idx)
     last_b, last_h = divmod(B * H - 1, H)
-    # first rows (tile 0 of the first CTA), last rows (its partner tile), and
-    # the rows around the middle of the sequence
-    dumps = [(0, 0, 0, 128), (last_b, last_h, N - 128, 128), (0, H - 1, N // 2 - 64, 128)]
+    mid_b, mid_h = divmod((B * H) // 2, H)
+    dumps = [(0, 0, 0, 128), (last_b, last_h, N - 128, 128), (mid_b, mid_h, N // 2 - 64, 128)]
     run_and_check(q, k, v, w.softmax_scale, dumps, sample, "causal workload %d" % idx, causal=True)
 
 

@@ -39,7 +39,7 @@ def _check_mxfp8(v, heads=None):
 def test_mxfp8_quantizer_bit_exact_on_workloads(idx):
     w = wl.WORKLOADS[idx]
     _, _, v = wl.make_inputs(w)
-    _check_mxfp8(v, heads=2 if idx == 4 else None)
+    _check_mxfp8(v)
     torch.cuda.empty_cache()
 
 
@@ -85,10 +85,10 @@ def test_fp8pv_workloads_sampled(idx, causal):
     w = wl.WORKLOADS[idx]
     q, k, v = wl.make_inputs(w)
     B, H, N, D = w.shape
-    heads = sorted({0, B * H - 1})
-    sample = sample_rows(B, H, N, heads, 24 if idx == 4 else 48, seed=300 + idx)
+    sample = sample_rows(B, H, N, range(B * H), 16 if idx in (4, 5) else 32, seed=300 + idx)
     last_b, last_h = divmod(B * H - 1, H)
-    dumps = [(0, 0, 0, 64), (last_b, last_h, N - 64, 64)]
+    mid_b, mid_h = divmod((B * H) // 2, H)
+    dumps = [(0, 0, 0, 64), (last_b, last_h, N - 64, 64), (mid_b, mid_h, N // 2 - 64, 128)]
     run_and_check(q, k, v, w.softmax_scale, dumps, sample, "fp8pv workload %d causal=%d" % (idx, causal),
                   causal=causal, fp8pv=True)
 
