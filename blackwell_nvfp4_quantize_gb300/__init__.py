@@ -84,7 +84,10 @@ def lib():
                                              vp, vp]
     L.fp4attn_debug_wait_timeout.argtypes = [i, vp]
     L.fp4attn_debug_mma_peak.argtypes = [i, i, vp]
-    for name in ("fp4attn_debug_wait_timeout", "fp4attn_debug_mma_peak", "fp4attn_mxfp8_v_bytes", "fp4attn_quant_v_mxfp8", "fp4attn_fwd_directp_fp8pv",
+    L.fp4attn_debug_noalloc_timeout.argtypes = [vp, ctypes.c_longlong, i, vp]
+    L.fp4attn_debug_status_word_exists.argtypes = [ctypes.POINTER(i)]
+    for name in ("fp4attn_debug_wait_timeout", "fp4attn_debug_mma_peak", "fp4attn_debug_noalloc_timeout",
+                 "fp4attn_debug_status_word_exists", "fp4attn_mxfp8_v_bytes", "fp4attn_quant_v_mxfp8", "fp4attn_fwd_directp_fp8pv",
                  "fp4attn_debug_dump_p_fp8pv", "fp4attn_fwd_directp_causal", "fp4attn_debug_dump_p_causal", "fp4attn_fwd_directp_causal_save",
                  "fp4attn_fwd_directp_noalloc", "fp4attn_debug_cvt_transitions", "fp4attn_nvfp4_bytes", "fp4attn_mxfp4_v_bytes", "fp4attn_quant_qk_nvfp4",
                  "fp4attn_quant_v_mxfp4", "fp4attn_fwd_directp", "fp4attn_debug_dump_p",
@@ -365,6 +368,8 @@ def fwd_directp_noalloc(q: NVFP4Tensor, k: NVFP4Tensor, v: MXFP4Tensor, o: torch
     """fp4attn_fwd_directp_noalloc: the same forward with no device allocation
     anywhere on its path; the caller provides O and LSE.  A bounded wait that
     gives up shows as NaN in every LSE entry instead of a status code."""
+    if o is None or lse is None:
+        raise ValueError("fwd_directp_noalloc writes into caller-provided o and lse: both are required")
     _check_fwd_args(q, k, v, MXFP4Tensor, o, lse)
     B, H, N, D = q.shape
     if softmax_scale is None:
@@ -413,6 +418,24 @@ def debug_dump_p(q: NVFP4Tensor, k: NVFP4Tensor, v, b: int, h: int, row0: int, n
 def device_status(stream=None) -> int:
     """fp4attn_device_status: FP4ATTN_OK, or FP4ATTN_ERR_TIMEOUT if a bounded wait gave up."""
     return lib().fp4attn_device_status(ctypes.c_void_p(_stream(stream)))
+
+
+def debug_noalloc_timeout(lse: torch.Tensor, limit_us: int, stream=None) -> None:
+    """fp4attn_debug_noalloc_timeout: a bounded wait on the allocation-free
+    entry point's status word gives up after limit_us, and its report kernel
+    sets every entry of lse (a CUDA fp32 tensor) to NaN."""
+    if not (isinstance(lse, torch.Tensor) and lse.is_cuda and lse.dtype == torch.float32 and lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous CUDA fp32 tensor")
+    _check(lib().fp4attn_debug_noalloc_timeout(_ptr(lse), lse.numel(), int(limit_us), ctypes.c_void_p(_stream(stream))),
+           "fp4attn_debug_noalloc_timeout")
+
+
+def debug_status_word_exists() -> bool:
+    """fp4attn_debug_status_word_exists: has the library created its
+    per-device status block on the current device?"""
+    e = ctypes.c_int(-1)
+    _check(lib().fp4attn_debug_status_word_exists(ctypes.byref(e)), "fp4attn_debug_status_word_exists")
+    return bool(e.value)
 
 
 def debug_wait_timeout(limit_us: int, stream=None) -> None:

@@ -95,3 +95,12 @@ extern "C" int fp4attn_device_status(void* stream) {
   }
   return FP4ATTN_OK;
 }
+
+extern "C" int fp4attn_debug_status_word_exists(int* exists) {
+  if (!exists) return FP4ATTN_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP4ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  *exists = g_status[dev] != nullptr ? 1 : 0;
+  return FP4ATTN_OK;
+}

@@ -746,12 +746,14 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 
 // v: the V payload and scale atoms -- MXFP4 (E2M1) or, with P8, MXFP8 (E4M3)
 // V^T with one byte per key; both use the same atom layout.
+// status: the word the kernel's bounded waits report into -- the library's
+// per-device status block, or the allocation-free entry point's static word;
+// it is never created here.
 template <int D, bool DUMP, bool CAUSAL = false, bool P8 = false>
 int launch(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k, const fp4attn_mxfp4_t* v, void* o, float* lse,
            int B, int H, int N, float softmax_scale, int dump_bh, int row0, int nrows, uint8_t* codes,
-           int32_t* kshift, float* o_f32, cudaStream_t stream, DeviceStatus* status_word = nullptr) {
+           int32_t* kshift, float* o_f32, cudaStream_t stream, DeviceStatus* status) {
   using L = Layout<D, P8, CAUSAL && !P8>;
-  DeviceStatus* status = status_word ? status_word : device_status_ptr();
   if (!status) return FP4ATTN_ERR_CUDA;
   const int ntiles = n_row_tiles(N);
   const int BH = B * H;
@@ -830,8 +832,8 @@ extern "C" int fp4attn_fwd_directp(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4
   const int st = check_fwd(q, k, v, o, lse, B, H, N, D, softmax_scale);
   if (st != FP4ATTN_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (D == 128) return launch<128, false>(q, k, v, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr, nullptr, nullptr, s);
-  return launch<64, false>(q, k, v, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr, nullptr, nullptr, s);
+  if (D == 128) return launch<128, false>(q, k, v, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr, nullptr, nullptr, s, device_status_ptr());
+  return launch<64, false>(q, k, v, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr, nullptr, nullptr, s, device_status_ptr());
 }
 
 extern "C" int fp4attn_debug_dump_p(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k, const fp4attn_mxfp4_t* v,
@@ -845,8 +847,8 @@ extern "C" int fp4attn_debug_dump_p(const fp4attn_nvfp4_t* q, const fp4attn_nvfp
     return FP4ATTN_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int bh = b * H + h;
-  if (D == 128) return launch<128, true>(q, k, v, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes, kshift, o_f32, s);
-  return launch<64, true>(q, k, v, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes, kshift, o_f32, s);
+  if (D == 128) return launch<128, true>(q, k, v, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes, kshift, o_f32, s, device_status_ptr());
+  return launch<64, true>(q, k, v, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes, kshift, o_f32, s, device_status_ptr());
 }
 
 extern "C" int fp4attn_fwd_directp_causal(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k,
@@ -856,8 +858,8 @@ extern "C" int fp4attn_fwd_directp_causal(const fp4attn_nvfp4_t* q, const fp4att
   if (st != FP4ATTN_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (D == 128)
-    return launch<128, false, true>(q, k, v, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr, nullptr, nullptr, s);
-  return launch<64, false, true>(q, k, v, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr, nullptr, nullptr, s);
+    return launch<128, false, true>(q, k, v, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr, nullptr, nullptr, s, device_status_ptr());
+  return launch<64, false, true>(q, k, v, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr, nullptr, nullptr, s, device_status_ptr());
 }
 
 extern "C" int fp4attn_debug_dump_p_causal(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k,
@@ -878,8 +880,8 @@ extern "C" int fp4attn_debug_dump_p_causal(const fp4attn_nvfp4_t* q, const fp4at
     return FP4ATTN_ERR_CUDA;
   const int bh = b * H + h;
   if (D == 128)
-    return launch<128, true, true>(q, k, v, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes, kshift, o_f32, s);
-  return launch<64, true, true>(q, k, v, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes, kshift, o_f32, s);
+    return launch<128, true, true>(q, k, v, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes, kshift, o_f32, s, device_status_ptr());
+  return launch<64, true, true>(q, k, v, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes, kshift, o_f32, s, device_status_ptr());
 }
 
 extern "C" int fp4attn_fwd_directp_causal_save(const void* q, const void* k, const void* v,
@@ -912,13 +914,13 @@ extern "C" int fp4attn_fwd_directp_fp8pv(const fp4attn_nvfp4_t* q, const fp4attn
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (D == 128)
     return causal ? launch<128, false, true, true>(q, k, &vv, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr,
-                                                   nullptr, nullptr, s)
+                                                   nullptr, nullptr, s, device_status_ptr())
                   : launch<128, false, false, true>(q, k, &vv, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr,
-                                                    nullptr, nullptr, s);
+                                                    nullptr, nullptr, s, device_status_ptr());
   return causal ? launch<64, false, true, true>(q, k, &vv, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr,
-                                                nullptr, nullptr, s)
+                                                nullptr, nullptr, s, device_status_ptr())
                 : launch<64, false, false, true>(q, k, &vv, o, lse, B, H, N, softmax_scale, -1, 0, 0, nullptr,
-                                                 nullptr, nullptr, s);
+                                                 nullptr, nullptr, s, device_status_ptr());
 }
 
 extern "C" int fp4attn_debug_dump_p_fp8pv(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k,
@@ -942,13 +944,13 @@ extern "C" int fp4attn_debug_dump_p_fp8pv(const fp4attn_nvfp4_t* q, const fp4att
   const int bh = b * H + h;
   if (D == 128)
     return causal ? launch<128, true, true, true>(q, k, &vv, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes,
-                                                  kshift, o_f32, s)
+                                                  kshift, o_f32, s, device_status_ptr())
                   : launch<128, true, false, true>(q, k, &vv, o, lse, B, H, N, softmax_scale, bh, row0, nrows,
-                                                   codes, kshift, o_f32, s);
+                                                   codes, kshift, o_f32, s, device_status_ptr());
   return causal ? launch<64, true, true, true>(q, k, &vv, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes,
-                                               kshift, o_f32, s)
+                                               kshift, o_f32, s, device_status_ptr())
                 : launch<64, true, false, true>(q, k, &vv, o, lse, B, H, N, softmax_scale, bh, row0, nrows, codes,
-                                                kshift, o_f32, s);
+                                                kshift, o_f32, s, device_status_ptr());
 }
 
 // ------------------------------------------------------------------ allocation-free variant
@@ -991,6 +993,21 @@ __global__ void noalloc_report_timeout(const DeviceStatus* status, float* lse, l
     lse[i] = __int_as_float(0x7FC00000);
 }
 
+// Test support for the NaN report: one warp waits, through the forward's own
+// bounded wait, on an mbarrier that nothing arrives at, with a short limit,
+// so it gives up and records the timeout in the given status word.
+__global__ void __launch_bounds__(32) noalloc_wait_timeout_kernel(uint64_t limit_ns, DeviceStatus* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncwarp();
+  mbar_wait(&bar, 0, &abort_flag, status, 92, limit_ns);
+}
+
 }  // namespace
 }  // namespace fp4attn
 
@@ -1014,5 +1031,16 @@ extern "C" int fp4attn_fwd_directp_noalloc(const fp4attn_nvfp4_t* q, const fp4at
                                         status);
   if (r != FP4ATTN_OK) return r;
   noalloc_report_timeout<<<sm_count(), 256, 0, s>>>(status, lse, static_cast<long long>(B) * H * N);
+  return cuda_status(cudaGetLastError());
+}
+
+extern "C" int fp4attn_debug_noalloc_timeout(float* lse, long long n, int limit_us, void* stream) {
+  if (!lse || n <= 0 || !aligned16(lse) || limit_us <= 0 || limit_us > 1000000) return FP4ATTN_ERR_INVALID_ARG;
+  DeviceStatus* status = noalloc_status_word();
+  if (!status) return FP4ATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s) != cudaSuccess) return FP4ATTN_ERR_CUDA;
+  noalloc_wait_timeout_kernel<<<1, 32, 0, s>>>(static_cast<uint64_t>(limit_us) * 1000u, status);
+  noalloc_report_timeout<<<sm_count(), 256, 0, s>>>(status, lse, n);
   return cuda_status(cudaGetLastError());
 }

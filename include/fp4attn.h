@@ -224,6 +224,23 @@ int fp4attn_fwd_directp_noalloc(const fp4attn_nvfp4_t *q, const fp4attn_nvfp4_t 
                                 void *o, float *lse, int B, int H, int N, int D, float softmax_scale,
                                 void *stream);
 
+/* Test support for fp4attn_fwd_directp_noalloc (no counterpart in the paper):
+ * drives its failure report without a fault.  Clears the allocation-free
+ * entry point's static status word, runs one warp whose bounded wait on an
+ * mbarrier that nothing completes gives up after limit_us microseconds
+ * (1 .. 10^6) and records the timeout in that word, then runs the same report
+ * kernel the entry point runs: every entry of lse[0 .. n) becomes NaN.  lse is
+ * a caller-owned fp32 device buffer, 16-byte aligned.  Allocates nothing;
+ * FP4ATTN_ERR_INVALID_ARG for a null/misaligned buffer or bad n / limit. */
+int fp4attn_debug_noalloc_timeout(float *lse, long long n, int limit_us, void *stream);
+
+/* Test support: *exists = 1 if the library has created its per-device status
+ * block (the one cudaMalloc of the library; see fp4attn_device_status) on the
+ * current device, 0 if not.  Lets a test show that a sequence of calls --
+ * the allocation-free forward above, the quantizers -- never created it.
+ * FP4ATTN_ERR_INVALID_ARG for a null pointer. */
+int fp4attn_debug_status_word_exists(int *exists);
+
 /* Same computation as fp4attn_fwd_directp (same kernel, same launch shape),
  * and in addition writes the probability codes, block shifts and fp32 output
  * of query rows row0 .. row0+nrows-1 of head (b, h):

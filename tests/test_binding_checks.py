@@ -81,3 +81,11 @@ def test_quantizer_inputs_and_outputs(fa):
         fa.quant_qk_nvfp4(x)
     with pytest.raises(ValueError, match="CUDA bf16"):
         fa.quant_v_mxfp4(x.float())
+
+
+def test_noalloc_needs_caller_outputs(fa):
+    B, H, N, D = SHAPE
+    with pytest.raises(ValueError, match="caller-provided"):
+        fa.fwd_directp_noalloc(_nv(fa), _nv(fa), _mx(fa), None, torch.zeros((B, H, N)))
+    with pytest.raises(ValueError, match="caller-provided"):
+        fa.fwd_directp_noalloc(_nv(fa), _nv(fa), _mx(fa), torch.zeros((B, H, N, D), dtype=torch.bfloat16), None)

@@ -143,3 +143,13 @@ def test_mma_peak_argument_errors(L):
     assert L.fp4attn_debug_mma_peak(-1, 16, None) == fa.FP4ATTN_ERR_INVALID_ARG
     assert L.fp4attn_debug_mma_peak(0, 0, None) == fa.FP4ATTN_ERR_INVALID_ARG
     assert L.fp4attn_debug_mma_peak(1, (1 << 26) + 1, None) == fa.FP4ATTN_ERR_INVALID_ARG
+
+
+def test_noalloc_debug_argument_errors(L):
+    import blackwell_nvfp4_quantize_gb300 as fa
+
+    assert L.fp4attn_debug_noalloc_timeout(None, 16, 100, None) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert L.fp4attn_debug_noalloc_timeout(ctypes.c_void_p(0x1008), 16, 100, None) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert L.fp4attn_debug_noalloc_timeout(ctypes.c_void_p(0x1000), 0, 100, None) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert L.fp4attn_debug_noalloc_timeout(ctypes.c_void_p(0x1000), 16, 0, None) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert L.fp4attn_debug_status_word_exists(None) == fa.FP4ATTN_ERR_INVALID_ARG
