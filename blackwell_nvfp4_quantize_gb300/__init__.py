@@ -86,6 +86,13 @@ def lib():
     L.fp4attn_debug_mma_peak.argtypes = [i, i, vp]
     L.fp4attn_debug_noalloc_timeout.argtypes = [vp, ctypes.c_longlong, i, vp]
     L.fp4attn_debug_status_word_exists.argtypes = [ctypes.POINTER(i)]
+    L.fp4attn_quant_mxfp8_t.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
+    L.fp4attn_quant_mxfp8_rows.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
+    L.fp4attn_mxfp8_rows_bytes.argtypes = [i, i, i, i, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+    L.fp4attn_bwd_workspace_bytes.argtypes = [i, i, i, i, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+    L.fp4attn_bwd_prep.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
+    L.fp4attn_bwd_directp_causal.argtypes = [ctypes.POINTER(_NVFP4), ctypes.POINTER(_NVFP4)] + \
+        [ctypes.POINTER(_MXFP4)] * 5 + [vp, vp, vp, vp, vp, i, i, i, i, ctypes.c_float, vp]
     for name in ("fp4attn_debug_wait_timeout", "fp4attn_debug_mma_peak", "fp4attn_debug_noalloc_timeout",
                  "fp4attn_debug_status_word_exists", "fp4attn_mxfp8_v_bytes", "fp4attn_quant_v_mxfp8", "fp4attn_fwd_directp_fp8pv",
                  "fp4attn_debug_dump_p_fp8pv", "fp4attn_fwd_directp_causal", "fp4attn_debug_dump_p_causal", "fp4attn_fwd_directp_causal_save",
@@ -489,3 +496,163 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scale: 
     vq = quant_v_mxfp4(v, stream=stream)
     fwd = fwd_directp_causal if causal else fwd_directp
     return fwd(qq, kq, vq, softmax_scale, stream=stream)
+
+
+# ---- causal backward ---------------------------------------------------------
+
+FP8_E4M3, FP8_E5M2 = 0, 1
+
+
+@dataclass
+class FP8Tensor:
+    """An MXFP8 operand of the backward: payload u8 and scale atoms u8.
+    layout "rows": [B,H,N,D] codes, blocks along D; "t": [B,H,D,Npad] codes,
+    blocks along the sequence.  fmt: FP8_E4M3 or FP8_E5M2."""
+    payload: torch.Tensor
+    sf: torch.Tensor
+    shape: tuple
+    layout: str
+    fmt: int
+
+    def _c(self):  # the C struct has the same two pointers as the MXFP4 one
+        return _MXFP4(self.payload.data_ptr(), self.sf.data_ptr())
+
+
+def mxfp8_rows_bytes(B, H, N, D):
+    p, s = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().fp4attn_mxfp8_rows_bytes(B, H, N, D, ctypes.byref(p), ctypes.byref(s)), "fp4attn_mxfp8_rows_bytes")
+    return p.value, s.value
+
+
+def bwd_workspace_bytes(B, H, N, D):
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().fp4attn_bwd_workspace_bytes(B, H, N, D, ctypes.byref(a), ctypes.byref(b)),
+           "fp4attn_bwd_workspace_bytes")
+    return a.value, b.value
+
+
+def empty_fp8(shape, layout: str, fmt: int, device) -> FP8Tensor:
+    B, H, N, D = shape
+    if layout == "rows":
+        pb, sb = mxfp8_rows_bytes(B, H, N, D)
+        payload = torch.empty((B, H, N, D), dtype=torch.uint8, device=device)
+    elif layout == "t":
+        pb, sb = mxfp8_v_bytes(B, H, N, D)
+        payload = torch.empty((B, H, D, (N + 127) // 128 * 128), dtype=torch.uint8, device=device)
+    else:
+        raise ValueError("layout must be 'rows' or 't'")
+    return FP8Tensor(payload, torch.empty((sb,), dtype=torch.uint8, device=device), tuple(shape), layout, fmt)
+
+
+def _check_fp8(t, name: str, shape, layout: str, fmt: int | None = None):
+    if not isinstance(t, FP8Tensor):
+        raise ValueError("%s must be an FP8Tensor" % name)
+    if tuple(t.shape) != tuple(shape) or t.layout != layout or (fmt is not None and t.fmt != fmt):
+        raise ValueError("%s must be a %s-layout %s FP8Tensor of shape %s" %
+                         (name, layout, {0: "E4M3", 1: "E5M2"}.get(fmt, "FP8"), tuple(shape)))
+    B, H, N, D = shape
+    pb, sb = (mxfp8_rows_bytes if layout == "rows" else mxfp8_v_bytes)(B, H, N, D)
+    dev = t.payload.device
+    _check_buffer(t.payload, name + ".payload", torch.uint8, pb, dev)
+    _check_buffer(t.sf, name + ".sf", torch.uint8, sb, dev)
+    return dev
+
+
+def _quant_fp8(name, layout, x, fmt, out, stream):
+    _check_input(x, "x")
+    if fmt not in (FP8_E4M3, FP8_E5M2):
+        raise ValueError("fmt must be FP8_E4M3 or FP8_E5M2")
+    B, H, N, D = x.shape
+    out = out or empty_fp8(x.shape, layout, fmt, x.device)
+    if _check_fp8(out, "out", x.shape, layout, fmt) != x.device:
+        raise ValueError("out must be on the device of x")
+    _check(getattr(lib(), name)(_ptr(x), _ptr(out.payload), _ptr(out.sf), int(fmt), B, H, N, D,
+                                ctypes.c_void_p(_stream(stream))), name)
+    return out
+
+
+def quant_mxfp8_rows(x: torch.Tensor, fmt: int, out: FP8Tensor | None = None, stream=None) -> FP8Tensor:
+    """fp4attn_quant_mxfp8_rows: MXFP8 along D, row-major."""
+    return _quant_fp8("fp4attn_quant_mxfp8_rows", "rows", x, fmt, out, stream)
+
+
+def quant_mxfp8_t(x: torch.Tensor, fmt: int, out: FP8Tensor | None = None, stream=None) -> FP8Tensor:
+    """fp4attn_quant_mxfp8_t: MXFP8 along the sequence, token-inner."""
+    return _quant_fp8("fp4attn_quant_mxfp8_t", "t", x, fmt, out, stream)
+
+
+def bwd_prep(o: torch.Tensor, dout: torch.Tensor, lse: torch.Tensor, l2: torch.Tensor | None = None,
+             delta: torch.Tensor | None = None, stream=None):
+    """fp4attn_bwd_prep: returns (l2, delta), fp32 [B,H,Npad] each."""
+    _check_input(o, "o")
+    _check_input(dout, "dout")
+    if o.shape != dout.shape or o.device != dout.device:
+        raise ValueError("o and dout must have one shape and device")
+    B, H, N, D = o.shape
+    _check_buffer(lse, "lse", torch.float32, B * H * N, o.device)
+    npad = (N + 127) // 128 * 128
+    l2 = l2 if l2 is not None else torch.empty((B, H, npad), dtype=torch.float32, device=o.device)
+    delta = delta if delta is not None else torch.empty((B, H, npad), dtype=torch.float32, device=o.device)
+    _check_buffer(l2, "l2", torch.float32, B * H * npad, o.device)
+    _check_buffer(delta, "delta", torch.float32, B * H * npad, o.device)
+    _check(lib().fp4attn_bwd_prep(_ptr(o), _ptr(dout), _ptr(lse), _ptr(l2), _ptr(delta), B, H, N, D,
+                                  ctypes.c_void_p(_stream(stream))), "fp4attn_bwd_prep")
+    return l2, delta
+
+
+def bwd_directp_causal(q_saved: NVFP4Tensor, k_saved: NVFP4Tensor, v_rows: FP8Tensor, do_rows: FP8Tensor,
+                       do_t: FP8Tensor, q_t: FP8Tensor, k_t: FP8Tensor, l2: torch.Tensor, delta: torch.Tensor,
+                       softmax_scale: float | None = None, dq: torch.Tensor | None = None,
+                       dk: torch.Tensor | None = None, dv: torch.Tensor | None = None, stream=None):
+    """fp4attn_bwd_directp_causal: returns (dQ, dK, dV), fp32 [B,H,N,D]."""
+    if not isinstance(q_saved, NVFP4Tensor):
+        raise ValueError("q_saved must be an NVFP4Tensor")
+    shape = tuple(q_saved.shape)
+    dev = _check_quantized(q_saved, "q_saved", shape, NVFP4Tensor)
+    if _check_quantized(k_saved, "k_saved", shape, NVFP4Tensor) != dev:
+        raise ValueError("the operands must be on one device")
+    for t, name, layout, fmt in ((v_rows, "v_rows", "rows", FP8_E4M3), (do_rows, "do_rows", "rows", FP8_E5M2),
+                                 (do_t, "do_t", "t", FP8_E5M2), (q_t, "q_t", "t", FP8_E4M3),
+                                 (k_t, "k_t", "t", FP8_E4M3)):
+        if _check_fp8(t, name, shape, layout, fmt) != dev:
+            raise ValueError("the operands must be on one device")
+    B, H, N, D = shape
+    npad = (N + 127) // 128 * 128
+    _check_buffer(l2, "l2", torch.float32, B * H * npad, dev)
+    _check_buffer(delta, "delta", torch.float32, B * H * npad, dev)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    outs = []
+    for t, name in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        t = t if t is not None else torch.empty((B, H, N, D), dtype=torch.float32, device=dev)
+        _check_buffer(t, name, torch.float32, B * H * N * D, dev)
+        outs.append(t)
+    if dev.type != "cuda":
+        raise ValueError("the operands must be CUDA tensors")
+    qc, kc = q_saved._c(), k_saved._c()
+    cs = [t._c() for t in (v_rows, do_rows, do_t, q_t, k_t)]
+    _check(lib().fp4attn_bwd_directp_causal(ctypes.byref(qc), ctypes.byref(kc), *[ctypes.byref(c) for c in cs],
+                                            _ptr(l2), _ptr(delta), *[_ptr(t) for t in outs], B, H, N, D,
+                                            float(softmax_scale), ctypes.c_void_p(_stream(stream))),
+           "fp4attn_bwd_directp_causal")
+    return tuple(outs)
+
+
+def attention_backward_causal(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                              lse: torch.Tensor, dout: torch.Tensor, q_saved: NVFP4Tensor, k_saved: NVFP4Tensor,
+                              softmax_scale: float | None = None, stream=None):
+    """The causal backward from the training forward's state (fwd_directp_causal_save: q_saved, k_saved, o,
+    lse) and the bf16 inputs q, k, v and output gradient dout: quantizes the FP8 operands (E4M3 V rows,
+    E5M2 dO rows and dO^T, E4M3 Q^T and K^T), computes l2 and Delta, and returns (dQ, dK, dV) fp32."""
+    for x, name in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        _check_input(x, name)
+        if x.shape != q.shape or x.device != q.device:
+            raise ValueError("q, k, v, o and dout must have one shape and device")
+    v_rows = quant_mxfp8_rows(v, FP8_E4M3, stream=stream)
+    do_rows = quant_mxfp8_rows(dout, FP8_E5M2, stream=stream)
+    do_t = quant_mxfp8_t(dout, FP8_E5M2, stream=stream)
+    q_t = quant_mxfp8_t(q, FP8_E4M3, stream=stream)
+    k_t = quant_mxfp8_t(k, FP8_E4M3, stream=stream)
+    l2, delta = bwd_prep(o, dout, lse, stream=stream)
+    return bwd_directp_causal(q_saved, k_saved, v_rows, do_rows, do_t, q_t, k_t, l2, delta, softmax_scale,
+                              stream=stream)

@@ -1,0 +1,62 @@
+// FP8 helpers of the backward operands: E4M3 / E5M2 conversion and the MX
+// block exponent (one E8M0 scale per 32 elements, no clipping of the block
+// maximum).
+#pragma once
+#include <cstdint>
+
+namespace fp4attn {
+
+constexpr int kFmtE4M3 = 0, kFmtE5M2 = 1;
+
+// Four fp32 values -> four FP8 codes (round to nearest even, saturating to
+// the largest finite value), x0 in the low byte.
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt_fp8x4(float x0, float x1, float x2, float x3) {
+  uint32_t r;
+  if constexpr (FMT == kFmtE4M3) {
+    asm("{\n.reg .b16 lo, hi;\n"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n"
+        "mov.b32 %0, {lo, hi};\n}\n"
+        : "=r"(r)
+        : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
+  } else {
+    asm("{\n.reg .b16 lo, hi;\n"
+        "cvt.rn.satfinite.e5m2x2.f32 lo, %2, %1;\n"
+        "cvt.rn.satfinite.e5m2x2.f32 hi, %4, %3;\n"
+        "mov.b32 %0, {lo, hi};\n}\n"
+        : "=r"(r)
+        : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
+  }
+  return r;
+}
+
+// Largest finite value of the format = 1.75 * 2^P.
+template <int FMT>
+constexpr int kFp8MaxExp = (FMT == kFmtE4M3) ? 8 : 15;
+
+// The smallest e >= -127 with amax <= 1.75 * 2^(P + e), from the bits of a
+// non-negative fp32 amax (f 2^k, f in [1, 2): e = k - P if f <= 1.75, else
+// k - P + 1; amax = 0 or below 2^-126 gives -127).
+template <int FMT>
+__device__ __forceinline__ int mx_exp_f32(float amax) {
+  const uint32_t a = __float_as_uint(amax);
+  const int ebits = static_cast<int>(a >> 23);
+  if (ebits == 0) return -127;
+  const int e = ebits - 127 - ((a & 0x7FFFFFu) <= 0x600000u ? kFp8MaxExp<FMT> : kFp8MaxExp<FMT> - 1);
+  return e < -127 ? -127 : e;
+}
+
+// The same from the bits of a non-negative bf16 amax (7 mantissa bits).
+template <int FMT>
+__device__ __forceinline__ int mx_exp_bf16(uint32_t m) {
+  const int ebits = static_cast<int>(m >> 7);
+  if (ebits == 0) return -127;
+  const int e = ebits - 127 - ((m & 0x7Fu) <= 0x60u ? kFp8MaxExp<FMT> : kFp8MaxExp<FMT> - 1);
+  return e < -127 ? -127 : e;
+}
+
+// 2^-e for -127 <= e <= 126, exact.
+__device__ __forceinline__ float pow2_neg(int e) { return __uint_as_float(static_cast<uint32_t>(127 - e) << 23); }
+
+}  // namespace fp4attn

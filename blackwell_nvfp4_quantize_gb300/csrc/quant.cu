@@ -7,9 +7,12 @@
 //  nvfp4_finalize     : g = amax / 2688 (1 for an all-zero tensor)
 //  mxfp4_v_kernel     : 32-key blocks per channel, E8M0 scale, codes written
 //                       key-inner (V transposed) through shared memory
-//  mxfp8_v_kernel     : the same for E4M3 codes (the FP8 P/V variant:
-//                       training keeps FP8 probabilities and values), one
-//                       byte per key
+//  mxfp8_t_kernel     : the same for FP8 codes, one byte per token: E4M3 V of
+//                       the FP8 P/V variant (training keeps FP8 probabilities
+//                       and values) and the backward's sequence-blocked
+//                       operands (E4M3 Q, K; E5M2 dO)
+//  mxfp8_rows_kernel  : 32-element blocks along D, FP8 codes row-major (the
+//                       backward's E4M3 V and E5M2 dO for dP = dO V^T)
 //
 // The data kernels are HBM-bound streaming passes: 16-byte vector loads with
 // 4 to 16 of them in flight per thread (a read stream on this GPU needs about
@@ -18,6 +21,7 @@
 // no multiply-add contraction changes a code.
 #include <cuda_bf16.h>
 
+#include "fp8.cuh"
 #include "internal.h"
 
 namespace fp4attn {
@@ -242,17 +246,18 @@ __global__ void __launch_bounds__(256) mxfp4_v_kernel(const uint4* __restrict__ 
         reinterpret_cast<const uint4*>(atom)[threadIdx.x];
 }
 
-// MXFP8 V: the same staging and atoms as mxfp4_v_kernel; the scale is the
-// smallest 2^e with amax <= 448 * 2^e and each key keeps one E4M3 byte.
-template <int D>
-__global__ void __launch_bounds__(256) mxfp8_v_kernel(const uint4* __restrict__ v, uint8_t* __restrict__ payload_t,
+// MXFP8 along the sequence, transposed: the same staging and atoms as
+// mxfp4_v_kernel; the scale is the smallest 2^e with amax <= fmt_max * 2^e
+// and each token keeps one FP8 byte.
+template <int D, int FMT>
+__global__ void __launch_bounds__(256) mxfp8_t_kernel(const uint4* __restrict__ v, uint8_t* __restrict__ payload_t,
                                                       uint8_t* __restrict__ sf, int N) {
   __shared__ __align__(16) uint16_t tile[128 * D];
   __shared__ __align__(16) uint32_t atom[128];
   const int kt = blockIdx.x;
   const long long bh = blockIdx.y;
   const int ntiles = gridDim.x;
-  const int npad = ntiles * 128;  // bytes per V^T row
+  const int npad = ntiles * 128;  // bytes per transposed row
   stage_v_tile<D>(v, tile, kt, bh, N);
   if (threadIdx.x < 128) atom[threadIdx.x] = 0u;
   __syncthreads();
@@ -267,19 +272,15 @@ __global__ void __launch_bounds__(256) mxfp8_v_kernel(const uint4* __restrict__ 
       uint32_t m = 0;
 #pragma unroll
       for (int i = 0; i < 32; ++i) m = max(m, (c ? (w2[i] >> 16) : w2[i]) & 0x7FFFu);
-      // e = smallest integer >= -127 with amax <= 448 * 2^e (448 = 1.75 * 2^8),
-      // from the bits of amax
-      const uint32_t ebits = m >> 7, frac = m & 0x7Fu;
-      int e = -127;
-      if (ebits != 0) e = max(-127, static_cast<int>(ebits) - 127 - (frac <= 0x60u ? 8 : 7));
-      const float inv_scale = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, e <= 121
+      const int e = mx_exp_bf16<FMT>(m);
+      const float inv_scale = pow2_neg(e);
       float y[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i)
         y[i] = __fmul_rn(__uint_as_float(c ? (w2[i] & 0xFFFF0000u) : (w2[i] << 16)), inv_scale);
       uint32_t wd[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) wd[i] = cvt_e4m3x4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
+      for (int i = 0; i < 8; ++i) wd[i] = cvt_fp8x4<FMT>(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
       uint4* dst = reinterpret_cast<uint4*>(payload_t + (bh * D + d) * npad + kt * 128 + kb * 32);
       __stcs(dst, make_uint4(wd[0], wd[1], wd[2], wd[3]));
       __stcs(dst + 1, make_uint4(wd[4], wd[5], wd[6], wd[7]));
@@ -290,6 +291,48 @@ __global__ void __launch_bounds__(256) mxfp8_v_kernel(const uint4* __restrict__ 
   if (threadIdx.x < 32)
     reinterpret_cast<uint4*>(sf + (bh * ntiles + kt) * 512)[threadIdx.x] =
         reinterpret_cast<const uint4*>(atom)[threadIdx.x];
+}
+
+// MXFP8 along D, row-major: one thread per 32-element block (four 16-byte
+// loads, 32 code bytes out); the block's scale byte goes to its row's atom
+// (row n % 128 of the (b, h, n / 128) atom, block d / 32).  The atoms are
+// cleared beforehand, so blocks past D and rows past N read 0.
+template <int D, int FMT>
+__global__ void __launch_bounds__(256) mxfp8_rows_kernel(const uint4* __restrict__ x, uint4* __restrict__ payload,
+                                                         uint8_t* __restrict__ sf, int N, long long nblocks) {
+  constexpr int KB = D / 32;
+  const int ntiles = (N + 127) / 128;
+  for (long long b = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; b < nblocks;
+       b += static_cast<long long>(gridDim.x) * blockDim.x) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = ld_stream(x + 4 * b + u);
+    uint32_t m2 = 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) m2 = absmax_vec(v[u], m2);
+    const int e = mx_exp_bf16<FMT>(max(m2 & 0xFFFFu, m2 >> 16));
+    const float inv_scale = pow2_neg(e);
+    uint32_t wd[8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      float y[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        y[2 * i] = __fmul_rn(__uint_as_float(w[i] << 16), inv_scale);
+        y[2 * i + 1] = __fmul_rn(__uint_as_float(w[i] & 0xFFFF0000u), inv_scale);
+      }
+      wd[2 * u] = cvt_fp8x4<FMT>(y[0], y[1], y[2], y[3]);
+      wd[2 * u + 1] = cvt_fp8x4<FMT>(y[4], y[5], y[6], y[7]);
+    }
+    __stcs(payload + 2 * b, make_uint4(wd[0], wd[1], wd[2], wd[3]));
+    __stcs(payload + 2 * b + 1, make_uint4(wd[4], wd[5], wd[6], wd[7]));
+    const long long row = b / KB;
+    const int kb = static_cast<int>(b % KB);
+    const long long bh = row / N;
+    const int n = static_cast<int>(row % N), r = n & 127;
+    sf[(bh * ntiles + (n >> 7)) * 512 + (r & 31) * 16 + (r >> 5) * 4 + kb] = static_cast<uint8_t>(e + 127);
+  }
 }
 
 int grid_for(long long work_items, int threads) {
@@ -341,15 +384,48 @@ extern "C" int fp4attn_quant_v_mxfp4(const void* v, uint8_t* payload_t, uint8_t*
 
 extern "C" int fp4attn_quant_v_mxfp8(const void* v, uint8_t* payload_t, uint8_t* sf, int B, int H, int N, int D,
                                      void* stream) {
+  return fp4attn_quant_mxfp8_t(v, payload_t, sf, FP4ATTN_FP8_E4M3, B, H, N, D, stream);
+}
+
+extern "C" int fp4attn_quant_mxfp8_t(const void* x, uint8_t* payload_t, uint8_t* sf, int fmt, int B, int H, int N,
+                                     int D, void* stream) {
   int st = check_shape(B, H, N, D);
   if (st != FP4ATTN_OK) return st;
-  if (!v || !payload_t || !sf) return FP4ATTN_ERR_INVALID_ARG;
-  if (!aligned16(v) || !aligned16(payload_t) || !aligned16(sf)) return FP4ATTN_ERR_INVALID_ARG;
+  if (!x || !payload_t || !sf) return FP4ATTN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(payload_t) || !aligned16(sf)) return FP4ATTN_ERR_INVALID_ARG;
+  if (fmt != FP4ATTN_FP8_E4M3 && fmt != FP4ATTN_FP8_E5M2) return FP4ATTN_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   dim3 grid(n_row_tiles(N), B * H);
-  if (D == 128)
-    mxfp8_v_kernel<128><<<grid, 256, 0, s>>>(static_cast<const uint4*>(v), payload_t, sf, N);
-  else
-    mxfp8_v_kernel<64><<<grid, 256, 0, s>>>(static_cast<const uint4*>(v), payload_t, sf, N);
+  const uint4* src = static_cast<const uint4*>(x);
+  if (D == 128) {
+    if (fmt == FP4ATTN_FP8_E4M3) mxfp8_t_kernel<128, kFmtE4M3><<<grid, 256, 0, s>>>(src, payload_t, sf, N);
+    else mxfp8_t_kernel<128, kFmtE5M2><<<grid, 256, 0, s>>>(src, payload_t, sf, N);
+  } else {
+    if (fmt == FP4ATTN_FP8_E4M3) mxfp8_t_kernel<64, kFmtE4M3><<<grid, 256, 0, s>>>(src, payload_t, sf, N);
+    else mxfp8_t_kernel<64, kFmtE5M2><<<grid, 256, 0, s>>>(src, payload_t, sf, N);
+  }
+  return cuda_status(cudaGetLastError());
+}
+
+extern "C" int fp4attn_quant_mxfp8_rows(const void* x, uint8_t* payload, uint8_t* sf, int fmt, int B, int H, int N,
+                                        int D, void* stream) {
+  int st = check_shape(B, H, N, D);
+  if (st != FP4ATTN_OK) return st;
+  if (!x || !payload || !sf) return FP4ATTN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(payload) || !aligned16(sf)) return FP4ATTN_ERR_INVALID_ARG;
+  if (fmt != FP4ATTN_FP8_E4M3 && fmt != FP4ATTN_FP8_E5M2) return FP4ATTN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(sf, 0, mxfp4_sf_bytes(B, H, N, D), s) != cudaSuccess) return FP4ATTN_ERR_CUDA;
+  const long long nblocks = static_cast<long long>(B) * H * N * (D / 32);
+  const int grid = grid_for(nblocks, 256);
+  const uint4* src = static_cast<const uint4*>(x);
+  uint4* dst = reinterpret_cast<uint4*>(payload);
+  if (D == 128) {
+    if (fmt == FP4ATTN_FP8_E4M3) mxfp8_rows_kernel<128, kFmtE4M3><<<grid, 256, 0, s>>>(src, dst, sf, N, nblocks);
+    else mxfp8_rows_kernel<128, kFmtE5M2><<<grid, 256, 0, s>>>(src, dst, sf, N, nblocks);
+  } else {
+    if (fmt == FP4ATTN_FP8_E4M3) mxfp8_rows_kernel<64, kFmtE4M3><<<grid, 256, 0, s>>>(src, dst, sf, N, nblocks);
+    else mxfp8_rows_kernel<64, kFmtE5M2><<<grid, 256, 0, s>>>(src, dst, sf, N, nblocks);
+  }
   return cuda_status(cudaGetLastError());
 }

@@ -97,6 +97,21 @@ typedef struct {
     const uint8_t *sf;        /* scale atoms, fp4attn_mxfp8_v_bytes(...).sf bytes */
 } fp4attn_mxfp8_t;
 
+/* An MXFP8 operand of the backward: FP8 codes and their E8M0 scale atoms,
+ * either row-major (fp4attn_quant_mxfp8_rows: [B,H,N,D] bytes, blocks along
+ * D) or sequence-blocked and transposed (fp4attn_quant_mxfp8_t: [B,H,D,Npad]
+ * bytes, blocks along the sequence). */
+typedef struct {
+    const uint8_t *payload;
+    const uint8_t *sf;
+} fp4attn_fp8_t;
+
+/* FP8 code formats of the backward's operands. */
+enum {
+    FP4ATTN_FP8_E4M3 = 0, /* 4 exponent, 3 mantissa bits, largest 448 (OCP E4M3FN) */
+    FP4ATTN_FP8_E5M2 = 1  /* 5 exponent, 2 mantissa bits, largest 57344 */
+};
+
 /* Writable buffers of a quantized NVFP4 tensor (outputs of a call). */
 typedef struct {
     uint8_t *payload; /* [B,H,N,D/2] */
@@ -144,6 +159,71 @@ int fp4attn_quant_v_mxfp4(const void *v, uint8_t *payload_t, uint8_t *sf,
  * included).  One kernel; inputs must be finite. */
 int fp4attn_quant_v_mxfp8(const void *v, uint8_t *payload_t, uint8_t *sf,
                           int B, int H, int N, int D, void *stream);
+
+/* MXFP8-quantize a bf16 [B,H,N,D] tensor along the sequence, written
+ * token-inner: payload_t [B,H,D,Npad] bytes (tokens >= N: code 0) and the
+ * scale atoms of fp4attn_mxfp8_v_bytes, laid out as the V atoms (rows =
+ * channels, blocks = 32-token groups of each 128-token tile).  e is the
+ * smallest integer >= -127 with amax <= fmt_max * 2^e (fmt_max 448 for E4M3,
+ * 57344 for E5M2) and code = FP8(x * 2^-e), nearest, ties to even,
+ * saturating.  fmt: FP4ATTN_FP8_E4M3 or FP4ATTN_FP8_E5M2 (the backward's
+ * E4M3 Q and K and E5M2 output gradient dO; "What the paper found": the
+ * backward uses FP8 gradient operands, including E5M2 output gradients).
+ * fp4attn_quant_v_mxfp8 is this call with E4M3.  One kernel. */
+int fp4attn_quant_mxfp8_t(const void *x, uint8_t *payload_t, uint8_t *sf, int fmt,
+                          int B, int H, int N, int D, void *stream);
+
+/* Sizes of the row-major MXFP8 buffers: payload B*H*N*D bytes, scale atoms
+ * as fp4attn_mxfp8_v_bytes. */
+int fp4attn_mxfp8_rows_bytes(int B, int H, int N, int D, size_t *payload_bytes, size_t *sf_bytes);
+
+/* MXFP8-quantize a bf16 [B,H,N,D] tensor along D, row-major: payload
+ * [B,H,N,D] bytes; scale atom [b*H + h][n / 128], row n % 128, block d / 32
+ * (blocks d >= D and rows n >= N hold 0).  Same scale rule and codes as
+ * fp4attn_quant_mxfp8_t.  The backward's E4M3 V and E5M2 dO for the
+ * dP = dO V^T product.  A memset of sf and one kernel. */
+int fp4attn_quant_mxfp8_rows(const void *x, uint8_t *payload, uint8_t *sf, int fmt,
+                             int B, int H, int N, int D, void *stream);
+
+/* Sizes of the backward's two per-row fp32 arrays (l2, delta):
+ * B*H*Npad floats each, Npad = N rounded up to a multiple of 128. */
+int fp4attn_bwd_workspace_bytes(int B, int H, int N, int D, size_t *l2_bytes, size_t *delta_bytes);
+
+/* First step of the causal backward: delta[b,h,n] = sum_d dO * O (fp32
+ * accumulation of the bf16 products) and l2[b,h,n] = fp32(lse * fp32(log2 e))
+ * into [B,H,Npad] arrays, with l2 = +inf and delta = 0 for n >= N.
+ * o, dout: bf16 [B,H,N,D]; lse: fp32 [B,H,N] as the causal forward wrote it.
+ * One kernel. */
+int fp4attn_bwd_prep(const void *o, const void *dout, const float *lse, float *l2, float *delta,
+                     int B, int H, int N, int D, void *stream);
+
+/* Causal Direct-P backward ("What the paper found": the backward
+ * reconstructs the probabilities from the saved quantized Q/K payloads,
+ * scales and LSE values and uses FP8 gradient operands, including E5M2
+ * output gradients).  Computes, for query i and key j <= i,
+ *   P_ij  = 2^(fp32(c S_ij - l2_i))   (c, S: the forward's score multiplier
+ *                                      and block-scaled NVFP4 product of q, k;
+ *                                      ex2 flushes results below 2^-126)
+ *   dP_ij = dO~_i . V~_j              (E5M2 dO and E4M3 V, blocks along D)
+ *   dS_ij = P_ij (dP_ij - delta_i)    (fp32)
+ *   dV_j  = sum_i P~_ij dO~_i                  P~ E4M3, blocks of 32 queries
+ *   dK_j  = softmax_scale sum_i dS~_ij Q~_i     dS~ E5M2, blocks of 32 queries
+ *   dQ_i  = softmax_scale sum_j dS~_ij K~_j     dS~ E5M2, blocks of 32 keys
+ * where X~ is MX block quantization (E8M0 scale per 32 elements along each
+ * product's contraction axis, the rule of fp4attn_quant_mxfp8_t).
+ * q, k: the NVFP4 tensors the causal forward consumed (saved);
+ * v_rows: E4M3 fp4attn_quant_mxfp8_rows of V; do_rows: E5M2 rows of dO;
+ * do_t: E5M2 fp4attn_quant_mxfp8_t of dO; q_t, k_t: E4M3
+ * fp4attn_quant_mxfp8_t of Q and K; l2, delta: from fp4attn_bwd_prep;
+ * dq, dk, dv: fp32 [B,H,N,D] outputs (every element written).
+ * softmax_scale: the forward's (finite, > 0).  Two kernel launches (keys
+ * stationary for dK and dV, queries stationary for dQ); errors as
+ * fp4attn_fwd_directp. */
+int fp4attn_bwd_directp_causal(const fp4attn_nvfp4_t *q, const fp4attn_nvfp4_t *k,
+                               const fp4attn_fp8_t *v_rows, const fp4attn_fp8_t *do_rows,
+                               const fp4attn_fp8_t *do_t, const fp4attn_fp8_t *q_t, const fp4attn_fp8_t *k_t,
+                               const float *l2, const float *delta, float *dq, float *dk, float *dv,
+                               int B, int H, int N, int D, float softmax_scale, void *stream);
 
 /* Noncausal Direct-P forward (abstract: "Direct-P for noncausal inference";
  * "What the paper found": E2M1 probability codes from log-softmax scores,

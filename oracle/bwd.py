@@ -16,7 +16,8 @@ operands).  The pages give no formula; the readings taken here:
   scaled product as the forward) and the saved LSE:
   P_ij = 2^(c S_ij - LSE_i log2 e), c = fp32(softmax_scale log2 e g_Q g_K),
   for keys j <= i, else 0.  The exponent is one fp32 FMA (c S - L_i) with
-  L_i = fp32(LSE_i * fp32(log2 e)); P_ij is fp32.
+  L_i = fp32(LSE_i * fp32(log2 e)); P_ij is fp32, values below 2^-126 flushed
+  to zero (the kernel's exponential flushes subnormal results).
 * Delta_i = sum_d dO_id O_id (fp32); dP = dO V^T; dS_ij = P_ij (dP_ij - Delta_i),
   the plain FlashAttention backward with P recomputed.
 * Every product runs on FP8 operands with MX block scaling (E8M0 scale per
@@ -220,6 +221,7 @@ def probabilities(s_raw, c32, l2, qi, kj):
     s32 = s_raw.astype(np.float32).astype(np.float64)
     arg = (np.float64(c32) * s32 - l2[qi].astype(np.float64)[:, None]).astype(np.float32)
     p = np.exp2(arg.astype(np.float64)).astype(np.float32)
+    p[p < np.float32(2.0 ** -126)] = 0.0  # the kernel's ex2 flushes subnormal results
     p[kj[None, :] > qi[:, None]] = 0.0
     return p
 
