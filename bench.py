@@ -337,6 +337,91 @@ def time_variant(w, causal, fp8pv, mma_peaks, dev, local, steps=10, warmup=3):
             "clocks": clocks.summary()}
 
 
+def backward_peak(peaks):
+    """The backward's five products: S on FP4 (kind::mxf4nvf4), dP, dV, dK, dQ
+    on FP8 (kind::mxf8f6f4), equal FLOPs each: the harmonic combination."""
+    return 1.0 / (0.2 / peaks["nvf4"] + 0.8 / peaks["mxf8"])
+
+
+def time_backward(w, mma_peaks, dev, local, steps=5, warmup=3):
+    """The causal backward at workload w: the training forward (quantize Q, K,
+    V; causal Direct-P; its O, LSE and saved NVFP4 Q/K) once, outside the
+    timed region, then per step the FP8 operand quantizers (E4M3 V rows,
+    E5M2 dO rows and dO^T, E4M3 Q^T, K^T), the prep pass and the two
+    backward kernels, with CUDA events around each step and around the
+    kernels.  Inputs exceed the L2 (no flush)."""
+    import torch
+
+    import blackwell_nvfp4_quantize_gb300 as fa
+    from blackwell_nvfp4_quantize_gb300 import workloads as wl
+
+    B, H, N, D = w.shape
+    stream = torch.cuda.current_stream()
+    q, k, v = (t.to(dev) for t in wl.make_inputs(w))
+    g = torch.Generator().manual_seed(5000 + w.index)
+    dout = torch.randn((B, H, N, D), generator=g).to(torch.bfloat16).to(dev)
+    o, lse, q_saved, k_saved, _ = fa.fwd_directp_causal_save(q, k, v, w.softmax_scale, stream=stream)
+    bufs = {"v_rows": fa.empty_fp8(w.shape, "rows", fa.FP8_E4M3, dev),
+            "do_rows": fa.empty_fp8(w.shape, "rows", fa.FP8_E5M2, dev),
+            "do_t": fa.empty_fp8(w.shape, "t", fa.FP8_E5M2, dev),
+            "q_t": fa.empty_fp8(w.shape, "t", fa.FP8_E4M3, dev),
+            "k_t": fa.empty_fp8(w.shape, "t", fa.FP8_E4M3, dev)}
+    npad = (N + 127) // 128 * 128
+    l2 = torch.empty((B, H, npad), dtype=torch.float32, device=dev)
+    delta = torch.empty_like(l2)
+    grads = [torch.empty((B, H, N, D), dtype=torch.float32, device=dev) for _ in range(3)]
+
+    def step(ev=None):
+        fa.quant_mxfp8_rows(v, fa.FP8_E4M3, bufs["v_rows"], stream=stream)
+        fa.quant_mxfp8_rows(dout, fa.FP8_E5M2, bufs["do_rows"], stream=stream)
+        fa.quant_mxfp8_t(dout, fa.FP8_E5M2, bufs["do_t"], stream=stream)
+        fa.quant_mxfp8_t(q, fa.FP8_E4M3, bufs["q_t"], stream=stream)
+        fa.quant_mxfp8_t(k, fa.FP8_E4M3, bufs["k_t"], stream=stream)
+        fa.bwd_prep(o, dout, lse, l2, delta, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        fa.bwd_directp_causal(q_saved, k_saved, bufs["v_rows"], bufs["do_rows"], bufs["do_t"], bufs["q_t"],
+                              bufs["k_t"], l2, delta, w.softmax_scale, *grads, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    rec = []
+    with ClockSampler(local) as clocks:
+        for _ in range(steps):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            ev[2].record(stream)
+            step(ev)
+            ev[3].record(stream)
+            rec.append(ev)
+        torch.cuda.synchronize()
+    if fa.device_status() != fa.FP4ATTN_OK:
+        raise RuntimeError("device-side wait timed out in the backward")
+    step_ms = sum(e[2].elapsed_time(e[3]) for e in rec) / steps
+    kern_ms = sum(e[0].elapsed_time(e[1]) for e in rec) / steps
+    flops = 2.5 * B * H * attn_flops(range(N), N, D, True)  # 10*D per unmasked (query, key) pair
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+    peak = backward_peak(mma_peaks)
+    del q, k, v, dout, o, lse, q_saved, k_saved, bufs, l2, delta, grads
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "B": B, "H": H, "N": N, "D": D, "mask": "causal", "pass": "backward",
+            "steps": steps, "warmup": warmup,
+            "metric": "causal backward TFLOP/s (10*D per unmasked (query, key) pair: S, dP, dV, dK, dQ)",
+            "value": flops / (step_ms * 1e-3) / 1e12, "step_ms": step_ms, "bwd_kernels_ms": kern_ms,
+            "step": "E4M3 V rows, E5M2 dO rows and dO^T, E4M3 Q^T and K^T quantizers, prep (Delta, log2 LSE), "
+                    "key-stationary dK/dV kernel, query-stationary dQ kernel",
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "kernels": "bwd_kernel<%d, KV=true> + bwd_kernel<%d, KV=false>" % (D, D),
+                         "peak_source": "measured block-scaled MMA loop: 1/5 of the FLOPs on kind::mxf4nvf4 "
+                                        "(S), 4/5 on kind::mxf8f6f4 (dP, dV, dK, dQ), harmonic combination; "
+                                        "S and dP are computed twice (once per kernel) but counted once"},
+            "gpu_launches_per_step": 8,
+            "clocks": clocks.summary()}
+
+
 def run_mma_peak(args):
     """--mma-peak: the block-scaled tensor rates of this GPU and the clocks they ran at."""
     import torch
@@ -348,6 +433,21 @@ def run_mma_peak(args):
     line = {"mma_peak_tflops": peaks, "forward_peak_fp4": forward_peak(peaks, False),
             "forward_peak_fp8pv": forward_peak(peaks, True), "clocks": clocks.summary(),
             "shape": "M=128, N=128, K=128 per round (two K=64 E2M1 or four K=32 E4M3 products), one CTA per SM"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_bwd(args, w):
+    """--bwd: the causal backward line alone (measured peaks, then time_backward)."""
+    import torch
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    with ClockSampler(dev.index) as clocks:
+        peaks = measure_mma_peaks()
+    line = time_backward(w, peaks, dev, dev.index, steps=args.steps, warmup=args.warmup)
+    line["peak_clocks"] = clocks.summary()
+    line["mma_peak_tflops"] = peaks
     print(json.dumps(line), flush=True)
     return 0
 
@@ -554,7 +654,8 @@ def run_ours(args, w):
         torch.cuda.empty_cache()
         line["variants"] = [time_variant(wl.WORKLOADS[5], False, False, mma_peaks, dev, local),
                             time_variant(w, True, False, mma_peaks, dev, local),
-                            time_variant(w, False, True, mma_peaks, dev, local)]
+                            time_variant(w, False, True, mma_peaks, dev, local),
+                            time_backward(w, mma_peaks, dev, local)]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, q_h, k_h, v_h, causal=args.causal, fp8pv=args.fp8pv)
     if rank == 0:
@@ -577,6 +678,8 @@ def main(argv=None):
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the D=64, causal and FP8 P/V forward timings of the default run")
     ap.add_argument("--mma-peak", action="store_true", help="print the measured block-scaled tensor rates and exit")
+    ap.add_argument("--bwd", action="store_true",
+                    help="time only the causal backward of the workload and print its line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -585,6 +688,8 @@ def main(argv=None):
     w = wl.WORKLOADS[args.workload]
     if args.mma_peak:
         return run_mma_peak(args)
+    if args.bwd:
+        return run_bwd(args, w)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

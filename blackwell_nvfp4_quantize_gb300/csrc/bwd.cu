@@ -23,9 +23,10 @@
 //       and the dV and dK accumulators stay in TMEM for the whole run.
 //   Q   one CTA per (128-query tile i, b*H+h), streaming the key tiles j <= i;
 //       rows are queries, one dQ accumulator.
-// Roles (192 threads): warps 0-3 one thread per row (= TMEM lane), warp 4
-// the TMA producer, warp 5 the MMA issuer and TMEM owner.  Every wait is
-// bounded (the library's status word records where one gave up).
+// Roles (320 threads): warps 0-7 row threads, two per row (= TMEM lane):
+// warps w and w+4 take columns 0-63 and 64-127 of the rows of lane quarter
+// w; warp 8 the TMA producer; warp 9 the MMA issuer and TMEM owner.  Every
+// wait is bounded (the library's status word records where one gave up).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -39,8 +40,9 @@
 namespace fp4attn {
 namespace {
 
-constexpr int kBwdThreads = 192;
-constexpr int kWarpLoad = 4, kWarpMma = 5;
+constexpr int kRowWarps = 8;  // two per TMEM lane quarter: each thread takes half of its row's 128 columns
+constexpr int kBwdThreads = 32 * kRowWarps + 64;
+constexpr int kWarpLoad = kRowWarps, kWarpMma = kRowWarps + 1;
 constexpr uint32_t kBwdTmemCols = 512;
 
 // kind::mxf8f6f4 instruction descriptor with the A and B formats (E4M3 0,
@@ -216,12 +218,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(bar_empty + s, 1);
     }
     mbar_init(bar_s_full, 1);
-    mbar_init(bar_pulled, 4);
+    mbar_init(bar_pulled, kRowWarps);
     mbar_init(bar_dp_full, 1);
-    mbar_init(bar_bank_free, 4);
-    mbar_init(bar_w1_full, 4);
+    mbar_init(bar_bank_free, kRowWarps);
+    mbar_init(bar_w1_full, kRowWarps);
     mbar_init(bar_w1_done, 1);
-    mbar_init(bar_w2_full, 4);
+    mbar_init(bar_w2_full, kRowWarps);
     mbar_init(bar_w2_done, 1);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
@@ -316,68 +318,93 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int a = 0; a < D / 64; ++a) tc_cp_sf_atom_warp(tmem + C::kSfA4 + 4 * a, smem_u32(smem + L::kSfA4 + a * 512));
       tc_cp_sf_atom_warp(tmem + C::kSfA8, smem_u32(smem + L::kAtA8));
     }
-    for (int t = 0; ok && t < nsteps; ++t) {
+    // S = A4 B4^T of step t into the bank (its stage has landed, the bank is free)
+    auto issue_s = [&](int t) {
       const int s = t % kStages;
-      uint8_t* big = smem + L::stage_big(s);
-      uint8_t* small = smem + L::stage_small(s);
-      if (!(ok = wait(bar_full + s, (t / kStages) & 1, 34))) break;
-      if (t > 0 && !(ok = wait(bar_bank_free, (t - 1) & 1, 35))) break;
+      if (!wait(bar_full + s, (t / kStages) & 1, 34)) return false;
+      if (t > 0 && !wait(bar_bank_free, (t - 1) & 1, 35)) return false;
       tc_fence_after();
-      // S = A4 B4^T into the bank
+      uint8_t* small = smem + L::stage_small(s);
 #pragma unroll
       for (int a = 0; a < D / 64; ++a)
         tc_cp_sf_atom_warp(tmem + C::kSfB4 + 4 * a, smem_u32(small + L::kSsB4 + a * 512));
-      const uint64_t b4 = smem_desc(smem_u32(big + L::kB4), 16, kSbo4, kSw4);
+      const uint64_t b4 = smem_desc(smem_u32(smem + L::stage_big(s) + L::kB4), 16, kSbo4, kSw4);
 #pragma unroll
       for (int ks = 0; ks < D / 64; ++ks)
         mma_nvf4_warp(bank, a4 + 2 * ks, b4 + 2 * ks, idesc_s, tmem + C::kSfA4 + 4 * ks, tmem + C::kSfB4 + 4 * ks,
                       ks > 0);
       tc_commit_warp(bar_s_full);
-      // dP = A8 B8^T into the same bank once the row threads hold S
-      if (!(ok = wait(bar_pulled, t & 1, 36))) break;
+      return true;
+    };
+    // dP = A8 B8^T of step t into the same bank once the row threads hold S
+    auto issue_dp = [&](int t) {
+      const int s = t % kStages;
+      if (!wait(bar_pulled, t & 1, 36)) return false;
       tc_fence_after();
-      tc_cp_sf_atom_warp(tmem + C::kSfB8, smem_u32(small + L::kSsB8));
-      const uint64_t b8 = smem_desc(smem_u32(big + L::kB8), 16, kSbo8, kSw8);
+      tc_cp_sf_atom_warp(tmem + C::kSfB8, smem_u32(smem + L::stage_small(s) + L::kSsB8));
+      const uint64_t b8 = smem_desc(smem_u32(smem + L::stage_big(s) + L::kB8), 16, kSbo8, kSw8);
 #pragma unroll
       for (int ks = 0; ks < D / 32; ++ks)
         mma_mxf8_warp(bank, a8 + 2 * ks, b8 + 2 * ks, idesc_mxf8_fmt(128, 128, kFmtA8, kFmtB8, ks, ks),
                       tmem + C::kSfA8, tmem + C::kSfB8, ks > 0);
       tc_commit_warp(bar_dp_full);
-      // acc0 += W1 T1^T  (KV: dV += P~^T dO, Q: dQ += dS~ K)
-      if (!(ok = wait(bar_w1_full, t & 1, 37))) break;
+      return true;
+    };
+    // acc0 += W1 T1^T  (KV: dV += P~^T dO, Q: dQ += dS~ K)
+    auto issue_w1 = [&](int t) {
+      const int s = t % kStages;
+      if (!wait(bar_w1_full, t & 1, 37)) return false;
       tc_fence_after();
       tc_cp_sf_atom_warp(tmem + C::kSfW1, smem_u32(smem + L::kAtW1));
-      tc_cp_sf_atom_warp(tmem + C::kSfT1, smem_u32(small + L::kSsT1));
-      const uint64_t t1 = smem_desc(smem_u32(big + L::kT1), 16, 1024, 2u);
+      tc_cp_sf_atom_warp(tmem + C::kSfT1, smem_u32(smem + L::stage_small(s) + L::kSsT1));
+      const uint64_t t1 = smem_desc(smem_u32(smem + L::stage_big(s) + L::kT1), 16, 1024, 2u);
       constexpr uint32_t kFmtW1 = KV ? kFmtE4M3 : kFmtE5M2, kFmtT1 = KV ? kFmtE5M2 : kFmtE4M3;
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
         mma_mxf8_warp(tmem + C::kAcc0, w1 + 2 * ks, t1 + 2 * ks, idesc_mxf8_fmt(128, D, kFmtW1, kFmtT1, ks, ks),
                       tmem + C::kSfW1, tmem + C::kSfT1, t > 0 || ks > 0);
       tc_commit_warp(bar_w1_done);
-      if constexpr (KV) {
-        // acc1 += W2 T2^T  (dK += dS~^T Q)
-        if (!(ok = wait(bar_w2_full, t & 1, 38))) break;
-        tc_fence_after();
-        tc_cp_sf_atom_warp(tmem + C::kSfW2, smem_u32(smem + L::kAtW2));
-        tc_cp_sf_atom_warp(tmem + C::kSfT2, smem_u32(small + L::kSsT2));
-        const uint64_t t2 = smem_desc(smem_u32(big + L::kT2), 16, 1024, 2u);
+      return true;
+    };
+    // KV: acc1 += W2 T2^T  (dK += dS~^T Q)
+    auto issue_w2 = [&](int t) {
+      const int s = t % kStages;
+      if (!wait(bar_w2_full, t & 1, 38)) return false;
+      tc_fence_after();
+      tc_cp_sf_atom_warp(tmem + C::kSfW2, smem_u32(smem + L::kAtW2));
+      tc_cp_sf_atom_warp(tmem + C::kSfT2, smem_u32(smem + L::stage_small(s) + L::kSsT2));
+      const uint64_t t2 = smem_desc(smem_u32(smem + L::stage_big(s) + L::kT2), 16, 1024, 2u);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_mxf8_warp(tmem + C::kAcc1, w2 + 2 * ks, t2 + 2 * ks, idesc_mxf8_fmt(128, D, kFmtE5M2, kFmtE4M3, ks, ks),
-                        tmem + C::kSfW2, tmem + C::kSfT2, t > 0 || ks > 0);
-        tc_commit_warp(bar_w2_done);
-      }
-      tc_commit_warp(bar_empty + s);
+      for (int ks = 0; ks < 4; ++ks)
+        mma_mxf8_warp(tmem + C::kAcc1, w2 + 2 * ks, t2 + 2 * ks, idesc_mxf8_fmt(128, D, kFmtE5M2, kFmtE4M3, ks, ks),
+                      tmem + C::kSfW2, tmem + C::kSfT2, t > 0 || ks > 0);
+      tc_commit_warp(bar_w2_done);
+      return true;
+    };
+    // Software pipeline: the next step's S goes into the bank as soon as the
+    // row threads have pulled this step's dP, ahead of this step's last
+    // products, and the next dP as soon as that S is pulled.
+    //   KV, step t: dV(t) [P~ is written early], S(t+1), dK(t), dP(t+1)
+    //   Q,  step t: S(t+1), dQ(t) [dS~ is written last], dP(t+1)
+    ok = ok && issue_s(0) && issue_dp(0);
+    for (int t = 0; ok && t < nsteps; ++t) {
+      const bool more = t + 1 < nsteps;
+      if (KV && !(ok = issue_w1(t))) break;
+      if (more && !(ok = issue_s(t + 1))) break;
+      if (!(ok = KV ? issue_w2(t) : issue_w1(t))) break;
+      tc_commit_warp(bar_empty + (t % kStages));
+      if (more && !(ok = issue_dp(t + 1))) break;
     }
     // every MMA and scale copy must be complete before TMEM is freed
     tc_commit_warp(bar_drain);
     mbar_wait_drain(bar_drain, 0, abort_flag, p.status, 39);
   } else {
     // ------------------------------------------------------------ row threads
-    const int row = threadIdx.x;  // == TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t t_bank = tmem + lane_base + C::kBank;
+    const int row = threadIdx.x & 127;  // == TMEM lane
+    const int half = warp >> 2;         // columns 64 half .. 64 half + 63
+    const int col0 = 64 * half;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t_bank = tmem + lane_base + C::kBank + col0;
     const int row_id = tile0 * 128 + row;  // KV: key, Q: query
     const float c = static_cast<float>(((static_cast<double>(p.softmax_scale) * 1.4426950408889634074) *
                                         static_cast<double>(*p.g_q)) * static_cast<double>(*p.g_k));
@@ -389,11 +416,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     uint8_t* w1_row = smem + L::kW1 + row * 128;
     uint8_t* w2_row = smem + L::kW2 + row * 128;
+    // this thread's two scale bytes of its row's atom word
+    const int at_off = (row & 31) * 16 + (row >> 5) * 4 + 2 * half;
     bool ok = true;
     for (int t = 0; t < nsteps; ++t) {
       const int s = t % kStages;
-      const float* st_l2 = reinterpret_cast<const float*>(smem + L::stage_small(s) + L::kSsL);
-      const float* st_delta = reinterpret_cast<const float*>(smem + L::stage_small(s) + L::kSsDelta);
+      const float* st_l2 = reinterpret_cast<const float*>(smem + L::stage_small(s) + L::kSsL) + col0;
+      const float* st_delta = reinterpret_cast<const float*>(smem + L::stage_small(s) + L::kSsDelta) + col0;
       const bool diag = streamed(t) == tile0;
       ok = mbar_wait(bar_s_full, t & 1, abort_flag, p.status, 40);
       // KV: this step's L and Delta are read from the stage, so the row
@@ -404,8 +433,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       tc_fence_after();
-      float pr[128];
-      tmem_ld128(t_bank, pr);
+      float pr[64];
+      tmem_ld32(t_bank, *reinterpret_cast<float(*)[32]>(pr));
+      tmem_ld32(t_bank + 32, *reinterpret_cast<float(*)[32]>(pr + 32));
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
@@ -413,10 +443,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // P = 2^(c S - L), one FMA and ex2 per element; causal mask on the
       // diagonal tile (KV: query col < key row; Q: key col > query row)
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
+      for (int i = 0; i < 64; ++i) {
         const float l = KV ? st_l2[i] : l2_row;
         float v = ex2_approx(fmaf(c, pr[i], -l));
-        if (diag && (KV ? (i < row) : (i > row))) v = 0.0f;
+        if (diag && (KV ? (col0 + i < row) : (col0 + i > row))) v = 0.0f;
         pr[i] = v;
       }
       if constexpr (KV) {
@@ -428,41 +458,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             break;
           }
         }
-        uint32_t sfw = 0;
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-          sfw |= static_cast<uint32_t>(mx_block_store<kFmtE4M3>(pr + 32 * b, w1_row, b, row) + 127) << (8 * b);
-        *reinterpret_cast<uint32_t*>(smem + L::kAtW1 + (row & 31) * 16 + (row >> 5) * 4) = sfw;
+        const int e0 = mx_block_store<kFmtE4M3>(pr, w1_row, 2 * half, row);
+        const int e1 = mx_block_store<kFmtE4M3>(pr + 32, w1_row, 2 * half + 1, row);
+        *reinterpret_cast<uint16_t*>(smem + L::kAtW1 + at_off) = static_cast<uint16_t>((e0 + 127) | ((e1 + 127) << 8));
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_w1_full);
       }
-      // dS = P (dP - Delta), E5M2 codes blocked along this row's columns
+      // dP to registers; the bank goes back for the next S at once
       ok = mbar_wait(bar_dp_full, t & 1, abort_flag, p.status, 42);
-      if (ok && t > 0) ok = mbar_wait(KV ? bar_w2_done : bar_w1_done, (t - 1) & 1, abort_flag, p.status, 43);
       if (!__all_sync(0xFFFFFFFFu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint8_t* ds_row = KV ? w2_row : w1_row;
-      uint32_t sfw = 0;
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        float dp[32];
-        tmem_ld32(t_bank + 32 * b, dp);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float dl = KV ? st_delta[32 * b + i] : delta_row;
-          dp[i] = __fmul_rn(pr[32 * b + i], __fsub_rn(dp[i], dl));
-        }
-        sfw |= static_cast<uint32_t>(mx_block_store<kFmtE5M2>(dp, ds_row, b, row) + 127) << (8 * b);
-      }
+      float dp[64];
+      tmem_ld32(t_bank, *reinterpret_cast<float(*)[32]>(dp));
+      tmem_ld32(t_bank + 32, *reinterpret_cast<float(*)[32]>(dp + 32));
+      tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_bank_free);
-      *reinterpret_cast<uint32_t*>(smem + (KV ? L::kAtW2 : L::kAtW1) + (row & 31) * 16 + (row >> 5) * 4) = sfw;
+      // dS = P (dP - Delta), E5M2 codes blocked along this row's columns
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const float dl = KV ? st_delta[i] : delta_row;
+        dp[i] = __fmul_rn(pr[i], __fsub_rn(dp[i], dl));
+      }
+      if (t > 0) {
+        ok = mbar_wait(KV ? bar_w2_done : bar_w1_done, (t - 1) & 1, abort_flag, p.status, 43);
+        if (!__all_sync(0xFFFFFFFFu, ok)) {
+          ok = false;
+          break;
+        }
+      }
+      uint8_t* ds_row = KV ? w2_row : w1_row;
+      const int e0 = mx_block_store<kFmtE5M2>(dp, ds_row, 2 * half, row);
+      const int e1 = mx_block_store<kFmtE5M2>(dp + 32, ds_row, 2 * half + 1, row);
+      *reinterpret_cast<uint16_t*>(smem + (KV ? L::kAtW2 : L::kAtW1) + at_off) =
+          static_cast<uint16_t>((e0 + 127) | ((e1 + 127) << 8));
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(KV ? bar_w2_full : bar_w1_full);
@@ -474,16 +508,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (__all_sync(0xFFFFFFFFu, ok)) {
       tc_fence_after();
       const bool store = row_id < N;
-      const size_t off = (static_cast<size_t>(bh) * N + (store ? row_id : 0)) * D;
+      // this thread writes channels D/2 half .. D/2 half + D/2 - 1 of its row
+      const size_t off = (static_cast<size_t>(bh) * N + (store ? row_id : 0)) * D + (D / 2) * half;
 #pragma unroll
       for (int acc = 0; acc < (KV ? 2 : 1); ++acc) {
         // KV: acc 0 = dV (unscaled), acc 1 = dK; Q: dQ
         const float scale = (KV && acc == 0) ? 1.0f : p.softmax_scale;
         float* dst = (acc == 0 ? p.out0 : p.out1) + off;
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = 0; cc < D / 64; ++cc) {
           float v[32];
-          tmem_ld32(tmem + lane_base + (acc == 0 ? C::kAcc0 : C::kAcc1) + 32 * cc, v);
+          tmem_ld32(tmem + lane_base + (acc == 0 ? C::kAcc0 : C::kAcc1) + (D / 2) * half + 32 * cc, v);
           tmem_wait_ld();
           if (store) {
 #pragma unroll
