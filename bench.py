@@ -367,8 +367,8 @@ def time_backward(w, mma_peaks, dev, local, steps=5, warmup=3):
             "q_t": fa.empty_fp8(w.shape, "t", fa.FP8_E4M3, dev),
             "k_t": fa.empty_fp8(w.shape, "t", fa.FP8_E4M3, dev)}
     npad = (N + 127) // 128 * 128
-    l2 = torch.empty((B, H, npad), dtype=torch.float32, device=dev)
-    delta = torch.empty_like(l2)
+    nl2 = torch.empty((B, H, npad), dtype=torch.float32, device=dev)
+    delta = torch.empty_like(nl2)
     grads = [torch.empty((B, H, N, D), dtype=torch.float32, device=dev) for _ in range(3)]
 
     def step(ev=None):
@@ -377,11 +377,11 @@ def time_backward(w, mma_peaks, dev, local, steps=5, warmup=3):
         fa.quant_mxfp8_t(dout, fa.FP8_E5M2, bufs["do_t"], stream=stream)
         fa.quant_mxfp8_t(q, fa.FP8_E4M3, bufs["q_t"], stream=stream)
         fa.quant_mxfp8_t(k, fa.FP8_E4M3, bufs["k_t"], stream=stream)
-        fa.bwd_prep(o, dout, lse, l2, delta, stream=stream)
+        fa.bwd_prep(o, dout, lse, nl2, delta, stream=stream)
         if ev is not None:
             ev[0].record(stream)
         fa.bwd_directp_causal(q_saved, k_saved, bufs["v_rows"], bufs["do_rows"], bufs["do_t"], bufs["q_t"],
-                              bufs["k_t"], l2, delta, w.softmax_scale, *grads, stream=stream)
+                              bufs["k_t"], nl2, delta, w.softmax_scale, *grads, stream=stream)
         if ev is not None:
             ev[1].record(stream)
 
@@ -404,7 +404,7 @@ def time_backward(w, mma_peaks, dev, local, steps=5, warmup=3):
     flops = 2.5 * B * H * attn_flops(range(N), N, D, True)  # 10*D per unmasked (query, key) pair
     achieved = flops / (kern_ms * 1e-3) / 1e12
     peak = backward_peak(mma_peaks)
-    del q, k, v, dout, o, lse, q_saved, k_saved, bufs, l2, delta, grads
+    del q, k, v, dout, o, lse, q_saved, k_saved, bufs, nl2, delta, grads
     torch.cuda.empty_cache()
     return {"workload": w.name, "B": B, "H": H, "N": N, "D": D, "mask": "causal", "pass": "backward",
             "steps": steps, "warmup": warmup,

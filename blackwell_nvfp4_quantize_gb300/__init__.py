@@ -581,9 +581,9 @@ def quant_mxfp8_t(x: torch.Tensor, fmt: int, out: FP8Tensor | None = None, strea
     return _quant_fp8("fp4attn_quant_mxfp8_t", "t", x, fmt, out, stream)
 
 
-def bwd_prep(o: torch.Tensor, dout: torch.Tensor, lse: torch.Tensor, l2: torch.Tensor | None = None,
+def bwd_prep(o: torch.Tensor, dout: torch.Tensor, lse: torch.Tensor, nl2: torch.Tensor | None = None,
              delta: torch.Tensor | None = None, stream=None):
-    """fp4attn_bwd_prep: returns (l2, delta), fp32 [B,H,Npad] each."""
+    """fp4attn_bwd_prep: returns (nl2, delta), fp32 [B,H,Npad] each (nl2 = -LSE log2 e)."""
     _check_input(o, "o")
     _check_input(dout, "dout")
     if o.shape != dout.shape or o.device != dout.device:
@@ -591,17 +591,17 @@ def bwd_prep(o: torch.Tensor, dout: torch.Tensor, lse: torch.Tensor, l2: torch.T
     B, H, N, D = o.shape
     _check_buffer(lse, "lse", torch.float32, B * H * N, o.device)
     npad = (N + 127) // 128 * 128
-    l2 = l2 if l2 is not None else torch.empty((B, H, npad), dtype=torch.float32, device=o.device)
+    nl2 = nl2 if nl2 is not None else torch.empty((B, H, npad), dtype=torch.float32, device=o.device)
     delta = delta if delta is not None else torch.empty((B, H, npad), dtype=torch.float32, device=o.device)
-    _check_buffer(l2, "l2", torch.float32, B * H * npad, o.device)
+    _check_buffer(nl2, "nl2", torch.float32, B * H * npad, o.device)
     _check_buffer(delta, "delta", torch.float32, B * H * npad, o.device)
-    _check(lib().fp4attn_bwd_prep(_ptr(o), _ptr(dout), _ptr(lse), _ptr(l2), _ptr(delta), B, H, N, D,
+    _check(lib().fp4attn_bwd_prep(_ptr(o), _ptr(dout), _ptr(lse), _ptr(nl2), _ptr(delta), B, H, N, D,
                                   ctypes.c_void_p(_stream(stream))), "fp4attn_bwd_prep")
-    return l2, delta
+    return nl2, delta
 
 
 def bwd_directp_causal(q_saved: NVFP4Tensor, k_saved: NVFP4Tensor, v_rows: FP8Tensor, do_rows: FP8Tensor,
-                       do_t: FP8Tensor, q_t: FP8Tensor, k_t: FP8Tensor, l2: torch.Tensor, delta: torch.Tensor,
+                       do_t: FP8Tensor, q_t: FP8Tensor, k_t: FP8Tensor, nl2: torch.Tensor, delta: torch.Tensor,
                        softmax_scale: float | None = None, dq: torch.Tensor | None = None,
                        dk: torch.Tensor | None = None, dv: torch.Tensor | None = None, stream=None):
     """fp4attn_bwd_directp_causal: returns (dQ, dK, dV), fp32 [B,H,N,D]."""
@@ -618,7 +618,7 @@ def bwd_directp_causal(q_saved: NVFP4Tensor, k_saved: NVFP4Tensor, v_rows: FP8Te
             raise ValueError("the operands must be on one device")
     B, H, N, D = shape
     npad = (N + 127) // 128 * 128
-    _check_buffer(l2, "l2", torch.float32, B * H * npad, dev)
+    _check_buffer(nl2, "nl2", torch.float32, B * H * npad, dev)
     _check_buffer(delta, "delta", torch.float32, B * H * npad, dev)
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
@@ -632,7 +632,7 @@ def bwd_directp_causal(q_saved: NVFP4Tensor, k_saved: NVFP4Tensor, v_rows: FP8Te
     qc, kc = q_saved._c(), k_saved._c()
     cs = [t._c() for t in (v_rows, do_rows, do_t, q_t, k_t)]
     _check(lib().fp4attn_bwd_directp_causal(ctypes.byref(qc), ctypes.byref(kc), *[ctypes.byref(c) for c in cs],
-                                            _ptr(l2), _ptr(delta), *[_ptr(t) for t in outs], B, H, N, D,
+                                            _ptr(nl2), _ptr(delta), *[_ptr(t) for t in outs], B, H, N, D,
                                             float(softmax_scale), ctypes.c_void_p(_stream(stream))),
            "fp4attn_bwd_directp_causal")
     return tuple(outs)
@@ -643,7 +643,7 @@ def attention_backward_causal(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                               softmax_scale: float | None = None, stream=None):
     """The causal backward from the training forward's state (fwd_directp_causal_save: q_saved, k_saved, o,
     lse) and the bf16 inputs q, k, v and output gradient dout: quantizes the FP8 operands (E4M3 V rows,
-    E5M2 dO rows and dO^T, E4M3 Q^T and K^T), computes l2 and Delta, and returns (dQ, dK, dV) fp32."""
+    E5M2 dO rows and dO^T, E4M3 Q^T and K^T), computes nl2 and Delta, and returns (dQ, dK, dV) fp32."""
     for x, name in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
         _check_input(x, name)
         if x.shape != q.shape or x.device != q.device:
@@ -653,6 +653,6 @@ def attention_backward_causal(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     do_t = quant_mxfp8_t(dout, FP8_E5M2, stream=stream)
     q_t = quant_mxfp8_t(q, FP8_E4M3, stream=stream)
     k_t = quant_mxfp8_t(k, FP8_E4M3, stream=stream)
-    l2, delta = bwd_prep(o, dout, lse, stream=stream)
-    return bwd_directp_causal(q_saved, k_saved, v_rows, do_rows, do_t, q_t, k_t, l2, delta, softmax_scale,
+    nl2, delta = bwd_prep(o, dout, lse, stream=stream)
+    return bwd_directp_causal(q_saved, k_saved, v_rows, do_rows, do_t, q_t, k_t, nl2, delta, softmax_scale,
                               stream=stream)

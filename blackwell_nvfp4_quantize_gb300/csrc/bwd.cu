@@ -132,7 +132,7 @@ struct BwdParams {
   const uint8_t* at_b8;  // streamed row atoms (KV: dO rows, Q: V rows)
   const uint8_t* at_t1;  // streamed transposed atoms (KV: dO^T, Q: K^T)
   const uint8_t* at_t2;  // KV: Q^T atoms
-  const float* l2;       // [B*H, Npad] LSE log2 e (+inf past N)
+  const float* nl2;      // [B*H, Npad] -LSE log2 e (-inf past N)
   const float* delta;    // [B*H, Npad] rowsum(dO o O) (0 past N)
   const float* g_q;
   const float* g_k;
@@ -157,16 +157,18 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
 // 128-byte row under the 128-byte swizzle (chunk c of row r at c ^ (r % 8)).
 template <int FMT>
 __device__ __forceinline__ int mx_block_store(const float* x, uint8_t* row_base, int blk, int row) {
-  float amax = 0.0f;
+  float amax = fabsf(x[0]);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  for (int i = 1; i < 31; i += 2) amax = fmax3(amax, fabsf(x[i]), fabsf(x[i + 1]));
+  amax = fmaxf(amax, fabsf(x[31]));
   const int e = mx_exp_f32<FMT>(amax);
   const float inv = pow2_neg(e);
+  float y[32];
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) fmul2(y[i], y[i + 1], x[i], x[i + 1], inv, inv);
   uint32_t w[8];
 #pragma unroll
-  for (int q = 0; q < 8; ++q)
-    w[q] = cvt_fp8x4<FMT>(__fmul_rn(x[4 * q], inv), __fmul_rn(x[4 * q + 1], inv), __fmul_rn(x[4 * q + 2], inv),
-                          __fmul_rn(x[4 * q + 3], inv));
+  for (int q = 0; q < 8; ++q) w[q] = cvt_fp8x4<FMT>(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
   const int c0 = 2 * blk, c1 = 2 * blk + 1;
   *reinterpret_cast<uint4*>(row_base + ((c0 ^ (row & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
   *reinterpret_cast<uint4*>(row_base + ((c1 ^ (row & 7)) * 16)) = make_uint4(w[4], w[5], w[6], w[7]);
@@ -283,7 +285,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_2d(big + L::kT2, &tm_t2, bar_full + s, u * 128, bh * D);
           bulk_load(small + L::kSsT2, p.at_t2 + at, 512, bar_full + s);
           const size_t lo = static_cast<size_t>(bh) * npad + static_cast<size_t>(u) * 128;
-          bulk_load(small + L::kSsL, p.l2 + lo, 512, bar_full + s);
+          bulk_load(small + L::kSsL, p.nl2 + lo, 512, bar_full + s);
           bulk_load(small + L::kSsDelta, p.delta + lo, 512, bar_full + s);
         }
       }
@@ -408,10 +410,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int row_id = tile0 * 128 + row;  // KV: key, Q: query
     const float c = static_cast<float>(((static_cast<double>(p.softmax_scale) * 1.4426950408889634074) *
                                         static_cast<double>(*p.g_q)) * static_cast<double>(*p.g_k));
-    // Q: this row's L and Delta
-    float l2_row = 0.0f, delta_row = 0.0f;
+    // Q: this row's -L and Delta
+    float nl2_row = 0.0f, delta_row = 0.0f;
     if constexpr (!KV) {
-      l2_row = p.l2[static_cast<size_t>(bh) * npad + row_id];
+      nl2_row = p.nl2[static_cast<size_t>(bh) * npad + row_id];
       delta_row = p.delta[static_cast<size_t>(bh) * npad + row_id];
     }
     uint8_t* w1_row = smem + L::kW1 + row * 128;
@@ -421,7 +423,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool ok = true;
     for (int t = 0; t < nsteps; ++t) {
       const int s = t % kStages;
-      const float* st_l2 = reinterpret_cast<const float*>(smem + L::stage_small(s) + L::kSsL) + col0;
+      const float* st_nl2 = reinterpret_cast<const float*>(smem + L::stage_small(s) + L::kSsL) + col0;
       const float* st_delta = reinterpret_cast<const float*>(smem + L::stage_small(s) + L::kSsDelta) + col0;
       const bool diag = streamed(t) == tile0;
       ok = mbar_wait(bar_s_full, t & 1, abort_flag, p.status, 40);
@@ -443,11 +445,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // P = 2^(c S - L), one FMA and ex2 per element; causal mask on the
       // diagonal tile (KV: query col < key row; Q: key col > query row)
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float l = KV ? st_l2[i] : l2_row;
-        float v = ex2_approx(fmaf(c, pr[i], -l));
-        if (diag && (KV ? (col0 + i < row) : (col0 + i > row))) v = 0.0f;
-        pr[i] = v;
+      for (int i = 0; i < 64; i += 2) {
+        ffma2(pr[i], pr[i + 1], c, c, pr[i], pr[i + 1], KV ? st_nl2[i] : nl2_row, KV ? st_nl2[i + 1] : nl2_row);
+        pr[i] = ex2_approx(pr[i]);
+        pr[i + 1] = ex2_approx(pr[i + 1]);
+      }
+      if (diag) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (KV ? (col0 + i < row) : (col0 + i > row)) pr[i] = 0.0f;
       }
       if constexpr (KV) {
         // P~^T: E4M3 codes blocked along the queries (this row's columns)
@@ -481,9 +487,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) mbar_arrive(bar_bank_free);
       // dS = P (dP - Delta), E5M2 codes blocked along this row's columns
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float dl = KV ? st_delta[i] : delta_row;
-        dp[i] = __fmul_rn(pr[i], __fsub_rn(dp[i], dl));
+      for (int i = 0; i < 64; i += 2) {
+        fsub2(dp[i], dp[i + 1], dp[i], dp[i + 1], KV ? st_delta[i] : delta_row, KV ? st_delta[i + 1] : delta_row);
+        fmul2(dp[i], dp[i + 1], pr[i], pr[i + 1], dp[i], dp[i + 1]);
       }
       if (t > 0) {
         ok = mbar_wait(KV ? bar_w2_done : bar_w1_done, (t - 1) & 1, abort_flag, p.status, 43);
@@ -540,13 +546,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-// Delta = rowsum(dO o O) in fp32 and L = fp32(LSE * fp32(log2 e)) into the
-// padded [B*H, Npad] arrays the backward kernels read (L = +inf, Delta = 0 past
-// N, so those queries get P = 0).  Eight lanes per row, one 16-byte load of dO
+// Delta = rowsum(dO o O) in fp32 and -L = -fp32(LSE * fp32(log2 e)) into the
+// padded [B*H, Npad] arrays the backward kernels read (-L = -inf, Delta = 0
+// past N, so those queries get P = 0); the exponent c S - L is then one FMA.  Eight lanes per row, one 16-byte load of dO
 // and of O per lane and step.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
-                                                       const float* __restrict__ lse, float* __restrict__ l2,
+                                                       const float* __restrict__ lse, float* __restrict__ nl2,
                                                        float* __restrict__ delta, int N, int npad,
                                                        long long rows_pad) {
   constexpr int VPR = D / 8;  // 16-byte vectors per row
@@ -573,7 +579,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__
     acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 4);
     if (sub == 0) {
       delta[r] = n < N ? acc : 0.0f;
-      l2[r] = n < N ? __fmul_rn(lse[bh * N + n], 1.4426950408889634f) : INFINITY;
+      nl2[r] = n < N ? -__fmul_rn(lse[bh * N + n], 1.4426950408889634f) : -INFINITY;
     }
   }
 }
@@ -645,7 +651,7 @@ int launch_bwd_kernel(const CUtensorMap& a4, const CUtensorMap& b4, const CUtens
 template <int D>
 int launch_bwd(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k, const fp4attn_fp8_t* v_rows,
                const fp4attn_fp8_t* do_rows, const fp4attn_fp8_t* do_t, const fp4attn_fp8_t* q_t,
-               const fp4attn_fp8_t* k_t, const float* l2, const float* delta, float* dq, float* dk, float* dv,
+               const fp4attn_fp8_t* k_t, const float* nl2, const float* delta, float* dq, float* dk, float* dv,
                int B, int H, int N, float softmax_scale, cudaStream_t stream, DeviceStatus* status) {
   const int BH = B * H, T = n_row_tiles(N), npad = T * 128;
   CUtensorMap mq, mk, mvr, mdor, mdot, mqt, mkt;
@@ -661,7 +667,7 @@ int launch_bwd(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k, const fp4attn
   kv.at_b8 = do_rows->sf;
   kv.at_t1 = do_t->sf;
   kv.at_t2 = q_t->sf;
-  kv.l2 = l2;
+  kv.nl2 = nl2;
   kv.delta = delta;
   kv.g_q = q->g;
   kv.g_k = k->g;
@@ -709,12 +715,12 @@ extern "C" int fp4attn_mxfp8_rows_bytes(int B, int H, int N, int D, size_t* payl
   return FP4ATTN_OK;
 }
 
-extern "C" int fp4attn_bwd_prep(const void* o, const void* dout, const float* lse, float* l2, float* delta, int B,
+extern "C" int fp4attn_bwd_prep(const void* o, const void* dout, const float* lse, float* nl2, float* delta, int B,
                                 int H, int N, int D, void* stream) {
   const int st = check_shape(B, H, N, D);
   if (st != FP4ATTN_OK) return st;
-  if (!o || !dout || !lse || !l2 || !delta) return FP4ATTN_ERR_INVALID_ARG;
-  if (!aligned16(o) || !aligned16(dout) || !aligned16(lse) || !aligned16(l2) || !aligned16(delta))
+  if (!o || !dout || !lse || !nl2 || !delta) return FP4ATTN_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(dout) || !aligned16(lse) || !aligned16(nl2) || !aligned16(delta))
     return FP4ATTN_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int npad = n_row_tiles(N) * 128;
@@ -724,9 +730,9 @@ extern "C" int fp4attn_bwd_prep(const void* o, const void* dout, const float* ls
   const int grid = static_cast<int>(want < cap ? want : cap);
   if (D == 128)
     bwd_prep_kernel<128><<<grid, 256, 0, s>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse,
-                                              l2, delta, N, npad, rows_pad);
+                                              nl2, delta, N, npad, rows_pad);
   else
-    bwd_prep_kernel<64><<<grid, 256, 0, s>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse, l2,
+    bwd_prep_kernel<64><<<grid, 256, 0, s>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse, nl2,
                                              delta, N, npad, rows_pad);
   return cuda_status(cudaGetLastError());
 }
@@ -734,7 +740,7 @@ extern "C" int fp4attn_bwd_prep(const void* o, const void* dout, const float* ls
 extern "C" int fp4attn_bwd_directp_causal(const fp4attn_nvfp4_t* q, const fp4attn_nvfp4_t* k,
                                           const fp4attn_fp8_t* v_rows, const fp4attn_fp8_t* do_rows,
                                           const fp4attn_fp8_t* do_t, const fp4attn_fp8_t* q_t,
-                                          const fp4attn_fp8_t* k_t, const float* l2, const float* delta, float* dq,
+                                          const fp4attn_fp8_t* k_t, const float* nl2, const float* delta, float* dq,
                                           float* dk, float* dv, int B, int H, int N, int D, float softmax_scale,
                                           void* stream) {
   const int st = check_shape(B, H, N, D);
@@ -744,7 +750,7 @@ extern "C" int fp4attn_bwd_directp_causal(const fp4attn_nvfp4_t* q, const fp4att
     return FP4ATTN_ERR_INVALID_ARG;
   if (!fp8_ok(v_rows) || !fp8_ok(do_rows) || !fp8_ok(do_t) || !fp8_ok(q_t) || !fp8_ok(k_t))
     return FP4ATTN_ERR_INVALID_ARG;
-  if (!l2 || !delta || !dq || !dk || !dv || !aligned16(l2) || !aligned16(delta) || !aligned16(dq) ||
+  if (!nl2 || !delta || !dq || !dk || !dv || !aligned16(nl2) || !aligned16(delta) || !aligned16(dq) ||
       !aligned16(dk) || !aligned16(dv))
     return FP4ATTN_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.0f) || !std::isfinite(softmax_scale)) return FP4ATTN_ERR_INVALID_ARG;
@@ -752,8 +758,8 @@ extern "C" int fp4attn_bwd_directp_causal(const fp4attn_nvfp4_t* q, const fp4att
   if (!status) return FP4ATTN_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (D == 128)
-    return launch_bwd<128>(q, k, v_rows, do_rows, do_t, q_t, k_t, l2, delta, dq, dk, dv, B, H, N, softmax_scale, s,
+    return launch_bwd<128>(q, k, v_rows, do_rows, do_t, q_t, k_t, nl2, delta, dq, dk, dv, B, H, N, softmax_scale, s,
                            status);
-  return launch_bwd<64>(q, k, v_rows, do_rows, do_t, q_t, k_t, l2, delta, dq, dk, dv, B, H, N, softmax_scale, s,
+  return launch_bwd<64>(q, k, v_rows, do_rows, do_t, q_t, k_t, nl2, delta, dq, dk, dv, B, H, N, softmax_scale, s,
                         status);
 }

@@ -56,6 +56,26 @@ __device__ __forceinline__ int mx_exp_bf16(uint32_t m) {
   return e < -127 ? -127 : e;
 }
 
+// (a0 * b0, a1 * b1) and (a0 - b0, a1 - b1), each rounded once (packed fp32).
+__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n.reg .b64 a, b, d;\n"
+      "mov.b64 a, {%2, %3};\n"
+      "mov.b64 b, {%4, %5};\n"
+      "mul.rn.f32x2 d, a, b;\n"
+      "mov.b64 {%0, %1}, d;\n}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void fsub2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n.reg .b64 a, b, d;\n"
+      "mov.b64 a, {%2, %3};\n"
+      "mov.b64 b, {%4, %5};\n"
+      "sub.rn.f32x2 d, a, b;\n"
+      "mov.b64 {%0, %1}, d;\n}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // 2^-e for -127 <= e <= 126, exact.
 __device__ __forceinline__ float pow2_neg(int e) { return __uint_as_float(static_cast<uint32_t>(127 - e) << 23); }
 

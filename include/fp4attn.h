@@ -185,23 +185,23 @@ int fp4attn_mxfp8_rows_bytes(int B, int H, int N, int D, size_t *payload_bytes, 
 int fp4attn_quant_mxfp8_rows(const void *x, uint8_t *payload, uint8_t *sf, int fmt,
                              int B, int H, int N, int D, void *stream);
 
-/* Sizes of the backward's two per-row fp32 arrays (l2, delta):
+/* Sizes of the backward's two per-row fp32 arrays (nl2, delta):
  * B*H*Npad floats each, Npad = N rounded up to a multiple of 128. */
-int fp4attn_bwd_workspace_bytes(int B, int H, int N, int D, size_t *l2_bytes, size_t *delta_bytes);
+int fp4attn_bwd_workspace_bytes(int B, int H, int N, int D, size_t *nl2_bytes, size_t *delta_bytes);
 
 /* First step of the causal backward: delta[b,h,n] = sum_d dO * O (fp32
- * accumulation of the bf16 products) and l2[b,h,n] = fp32(lse * fp32(log2 e))
- * into [B,H,Npad] arrays, with l2 = +inf and delta = 0 for n >= N.
- * o, dout: bf16 [B,H,N,D]; lse: fp32 [B,H,N] as the causal forward wrote it.
- * One kernel. */
-int fp4attn_bwd_prep(const void *o, const void *dout, const float *lse, float *l2, float *delta,
+ * accumulation of the bf16 products) and nl2[b,h,n] = -fp32(lse * fp32(log2 e))
+ * (the negated log2-domain LSE) into [B,H,Npad] arrays, with nl2 = -inf and
+ * delta = 0 for n >= N.  o, dout: bf16 [B,H,N,D]; lse: fp32 [B,H,N] as the
+ * causal forward wrote it.  One kernel. */
+int fp4attn_bwd_prep(const void *o, const void *dout, const float *lse, float *nl2, float *delta,
                      int B, int H, int N, int D, void *stream);
 
 /* Causal Direct-P backward ("What the paper found": the backward
  * reconstructs the probabilities from the saved quantized Q/K payloads,
  * scales and LSE values and uses FP8 gradient operands, including E5M2
  * output gradients).  Computes, for query i and key j <= i,
- *   P_ij  = 2^(fp32(c S_ij - l2_i))   (c, S: the forward's score multiplier
+ *   P_ij  = 2^(fp32(c S_ij + nl2_i))  (c, S: the forward's score multiplier
  *                                      and block-scaled NVFP4 product of q, k;
  *                                      ex2 flushes results below 2^-126)
  *   dP_ij = dO~_i . V~_j              (E5M2 dO and E4M3 V, blocks along D)
@@ -214,7 +214,7 @@ int fp4attn_bwd_prep(const void *o, const void *dout, const float *lse, float *l
  * q, k: the NVFP4 tensors the causal forward consumed (saved);
  * v_rows: E4M3 fp4attn_quant_mxfp8_rows of V; do_rows: E5M2 rows of dO;
  * do_t: E5M2 fp4attn_quant_mxfp8_t of dO; q_t, k_t: E4M3
- * fp4attn_quant_mxfp8_t of Q and K; l2, delta: from fp4attn_bwd_prep;
+ * fp4attn_quant_mxfp8_t of Q and K; nl2, delta: from fp4attn_bwd_prep;
  * dq, dk, dv: fp32 [B,H,N,D] outputs (every element written).
  * softmax_scale: the forward's (finite, > 0).  Two kernel launches (keys
  * stationary for dK and dV, queries stationary for dQ); errors as
@@ -222,7 +222,7 @@ int fp4attn_bwd_prep(const void *o, const void *dout, const float *lse, float *l
 int fp4attn_bwd_directp_causal(const fp4attn_nvfp4_t *q, const fp4attn_nvfp4_t *k,
                                const fp4attn_fp8_t *v_rows, const fp4attn_fp8_t *do_rows,
                                const fp4attn_fp8_t *do_t, const fp4attn_fp8_t *q_t, const fp4attn_fp8_t *k_t,
-                               const float *l2, const float *delta, float *dq, float *dk, float *dv,
+                               const float *nl2, const float *delta, float *dq, float *dk, float *dv,
                                int B, int H, int N, int D, float softmax_scale, void *stream);
 
 /* Noncausal Direct-P forward (abstract: "Direct-P for noncausal inference";

@@ -180,17 +180,17 @@ def test_prep(shape):
     B, H, N, D = shape
     o, do = _rand(shape, 1), _rand(shape, 2)
     lse = torch.randn((B, H, N), generator=torch.Generator().manual_seed(3)) * 5
-    l2, delta = fa.bwd_prep(o.cuda(), do.cuda(), lse.cuda())
+    nl2, delta = fa.bwd_prep(o.cuda(), do.cuda(), lse.cuda())
     want_delta, want_l2 = ob.prep(_bits(o), _bits(do), lse.numpy())
     npad = (N + 127) // 128 * 128
-    l2, delta = l2.cpu().numpy(), delta.cpu().numpy()
-    assert np.array_equal(l2[..., :N], want_l2)
-    assert np.all(np.isinf(l2[..., N:])) and np.all(l2[..., N:] > 0)
+    nl2, delta = nl2.cpu().numpy(), delta.cpu().numpy()
+    assert np.array_equal(nl2[..., :N], -want_l2)
+    assert np.all(np.isinf(nl2[..., N:])) and np.all(nl2[..., N:] < 0)
     assert np.all(delta[..., N:] == 0)
     # fp32 accumulation of D products: within D 2^-24 of the sum of |terms|
     mag = np.sum(np.abs(ob.bf16_to_f32(_bits(o)).astype(np.float64) * ob.bf16_to_f32(_bits(do))), axis=-1)
     assert np.all(np.abs(delta[..., :N] - want_delta) <= D * 2.0 ** -24 * mag + 1e-30)
-    assert l2.shape == (B, H, npad)
+    assert nl2.shape == (B, H, npad)
 
 
 # ---- the backward ------------------------------------------------------------
