@@ -108,13 +108,18 @@ struct BwdLayout {
                 "tiles keep 1024-B alignment");
 };
 
-// TMEM plan: the S / dP bank, the accumulators, the scale-factor columns.
-template <int D>
+// TMEM plan: the S and dP banks, the accumulators, the scale-factor
+// columns.  Where the columns allow (the dQ kernel, and the dK/dV kernel at
+// D = 64) S and dP have banks of their own; the dK/dV kernel at D = 128
+// passes both through one bank (S goes to registers before dP is computed).
+template <int D, bool KV>
 struct BwdCols {
-  static constexpr uint32_t kBank = 0;            // 128 fp32 columns
-  static constexpr uint32_t kAcc0 = 128;          // KV: dV, Q: dQ (D columns)
-  static constexpr uint32_t kAcc1 = 128 + D;      // KV: dK
-  static constexpr uint32_t kSfA4 = 128 + 2 * D;  // D/64 atoms of 4 columns
+  static constexpr bool kTwoBanks = !KV || D == 64;
+  static constexpr uint32_t kBankS = 0;                       // 128 fp32 columns
+  static constexpr uint32_t kBankDP = kTwoBanks ? 128 : 0;    // 128 fp32 columns
+  static constexpr uint32_t kAcc0 = kTwoBanks ? 256 : 128;    // KV: dV, Q: dQ (D columns)
+  static constexpr uint32_t kAcc1 = kAcc0 + D;                // KV: dK
+  static constexpr uint32_t kSfA4 = kAcc0 + (KV ? 2 * D : D);  // D/64 atoms of 4 columns
   static constexpr uint32_t kSfB4 = kSfA4 + 4 * (D / 64);
   static constexpr uint32_t kSfA8 = kSfB4 + 4 * (D / 64);
   static constexpr uint32_t kSfB8 = kSfA8 + 4;
@@ -182,7 +187,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                const __grid_constant__ CUtensorMap tm_t1, const __grid_constant__ CUtensorMap tm_t2,
                const BwdParams p) {
   using L = BwdLayout<D, KV>;
-  using C = BwdCols<D>;
+  using C = BwdCols<D, KV>;
   constexpr int kStages = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -191,9 +196,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* bar_full = bars + 1;
   uint64_t* bar_empty = bars + 1 + kStages;
   uint64_t* bar_s_full = bars + 1 + 2 * kStages;  // S (S^T) is in the bank
-  uint64_t* bar_pulled = bar_s_full + 1;          // the row threads hold S: the bank may take dP
-  uint64_t* bar_dp_full = bar_s_full + 2;         // dP (dP^T) is in the bank
-  uint64_t* bar_bank_free = bar_s_full + 3;       // dP pulled: the bank may take the next S
+  uint64_t* bar_pulled = bar_s_full + 1;          // the row threads hold S (one bank: it may take dP)
+  uint64_t* bar_dp_full = bar_s_full + 2;         // dP (dP^T) is in its bank
+  uint64_t* bar_bank_free = bar_s_full + 3;       // dP pulled (one bank: it may take the next S)
   uint64_t* bar_w1_full = bar_s_full + 4;         // W1 tile and atom written
   uint64_t* bar_w1_done = bar_s_full + 5;         // the product reading W1 is complete
   uint64_t* bar_w2_full = bar_s_full + 6;         // KV: W2 written
@@ -312,7 +317,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t a8 = smem_desc(smem_u32(smem + L::kA8), 16, kSbo8, kSw8);
     const uint64_t w1 = smem_desc(smem_u32(smem + L::kW1), 16, 1024, 2u);
     const uint64_t w2 = smem_desc(smem_u32(smem + L::kW2), 16, 1024, 2u);
-    const uint32_t bank = tmem + C::kBank;
+    const uint32_t bank_s = tmem + C::kBankS, bank_dp = tmem + C::kBankDP;
     bool ok = wait(bar_fixed, 0, 33);
     if (ok) {
       tc_fence_after();
@@ -324,7 +329,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     auto issue_s = [&](int t) {
       const int s = t % kStages;
       if (!wait(bar_full + s, (t / kStages) & 1, 34)) return false;
-      if (t > 0 && !wait(bar_bank_free, (t - 1) & 1, 35)) return false;
+      // the S bank is free once the row threads hold the previous S (two
+      // banks) or the previous dP (one bank)
+      if (t > 0 && !wait(C::kTwoBanks ? bar_pulled : bar_bank_free, (t - 1) & 1, 35)) return false;
       tc_fence_after();
       uint8_t* small = smem + L::stage_small(s);
 #pragma unroll
@@ -333,21 +340,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint64_t b4 = smem_desc(smem_u32(smem + L::stage_big(s) + L::kB4), 16, kSbo4, kSw4);
 #pragma unroll
       for (int ks = 0; ks < D / 64; ++ks)
-        mma_nvf4_warp(bank, a4 + 2 * ks, b4 + 2 * ks, idesc_s, tmem + C::kSfA4 + 4 * ks, tmem + C::kSfB4 + 4 * ks,
+        mma_nvf4_warp(bank_s, a4 + 2 * ks, b4 + 2 * ks, idesc_s, tmem + C::kSfA4 + 4 * ks, tmem + C::kSfB4 + 4 * ks,
                       ks > 0);
       tc_commit_warp(bar_s_full);
       return true;
     };
-    // dP = A8 B8^T of step t into the same bank once the row threads hold S
+    // dP = A8 B8^T of step t: into its own bank once the previous dP is
+    // pulled (two banks), or into the S bank once the row threads hold S
     auto issue_dp = [&](int t) {
       const int s = t % kStages;
-      if (!wait(bar_pulled, t & 1, 36)) return false;
+      if (C::kTwoBanks ? (t > 0 && !wait(bar_bank_free, (t - 1) & 1, 36)) : !wait(bar_pulled, t & 1, 36))
+        return false;
       tc_fence_after();
       tc_cp_sf_atom_warp(tmem + C::kSfB8, smem_u32(smem + L::stage_small(s) + L::kSsB8));
       const uint64_t b8 = smem_desc(smem_u32(smem + L::stage_big(s) + L::kB8), 16, kSbo8, kSw8);
 #pragma unroll
       for (int ks = 0; ks < D / 32; ++ks)
-        mma_mxf8_warp(bank, a8 + 2 * ks, b8 + 2 * ks, idesc_mxf8_fmt(128, 128, kFmtA8, kFmtB8, ks, ks),
+        mma_mxf8_warp(bank_dp, a8 + 2 * ks, b8 + 2 * ks, idesc_mxf8_fmt(128, 128, kFmtA8, kFmtB8, ks, ks),
                       tmem + C::kSfA8, tmem + C::kSfB8, ks > 0);
       tc_commit_warp(bar_dp_full);
       return true;
@@ -383,19 +392,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_commit_warp(bar_w2_done);
       return true;
     };
-    // Software pipeline: the next step's S goes into the bank as soon as the
-    // row threads have pulled this step's dP, ahead of this step's last
-    // products, and the next dP as soon as that S is pulled.
-    //   KV, step t: dV(t) [P~ is written early], S(t+1), dK(t), dP(t+1)
-    //   Q,  step t: S(t+1), dQ(t) [dS~ is written last], dP(t+1)
+    // Software pipeline: each product is issued as soon as its bank and
+    // operands are ready, ahead of the current step's last products.
+    //   one bank,  KV step t: dV(t) [P~ is written early], S(t+1) [after the
+    //              dP(t) pull], dK(t), dP(t+1) [after the S(t+1) pull]
+    //   two banks, KV step t: S(t+1) [after the S(t) pull], dV(t), dP(t+1)
+    //              [after the dP(t) pull], dK(t)
+    //   two banks, Q  step t: S(t+1), dP(t+1), dQ(t) [dS~ is written last]
     ok = ok && issue_s(0) && issue_dp(0);
     for (int t = 0; ok && t < nsteps; ++t) {
       const bool more = t + 1 < nsteps;
-      if (KV && !(ok = issue_w1(t))) break;
-      if (more && !(ok = issue_s(t + 1))) break;
-      if (!(ok = KV ? issue_w2(t) : issue_w1(t))) break;
-      tc_commit_warp(bar_empty + (t % kStages));
-      if (more && !(ok = issue_dp(t + 1))) break;
+      if constexpr (C::kTwoBanks) {
+        if (more && !(ok = issue_s(t + 1))) break;
+        if (KV && !(ok = issue_w1(t))) break;
+        if (more && !(ok = issue_dp(t + 1))) break;
+        if (!(ok = KV ? issue_w2(t) : issue_w1(t))) break;
+        tc_commit_warp(bar_empty + (t % kStages));
+      } else {
+        if (!(ok = issue_w1(t))) break;
+        if (more && !(ok = issue_s(t + 1))) break;
+        if (!(ok = issue_w2(t))) break;
+        tc_commit_warp(bar_empty + (t % kStages));
+        if (more && !(ok = issue_dp(t + 1))) break;
+      }
     }
     // every MMA and scale copy must be complete before TMEM is freed
     tc_commit_warp(bar_drain);
@@ -406,7 +425,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int half = warp >> 2;         // columns 64 half .. 64 half + 63
     const int col0 = 64 * half;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t t_bank = tmem + lane_base + C::kBank + col0;
+    const uint32_t t_bank = tmem + lane_base + C::kBankS + col0;
+    const uint32_t t_dpbank = tmem + lane_base + C::kBankDP + col0;
     const int row_id = tile0 * 128 + row;  // KV: key, Q: query
     const float c = static_cast<float>(((static_cast<double>(p.softmax_scale) * 1.4426950408889634074) *
                                         static_cast<double>(*p.g_q)) * static_cast<double>(*p.g_k));
@@ -479,8 +499,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       tc_fence_after();
       float dp[64];
-      tmem_ld32(t_bank, *reinterpret_cast<float(*)[32]>(dp));
-      tmem_ld32(t_bank + 32, *reinterpret_cast<float(*)[32]>(dp + 32));
+      tmem_ld32(t_dpbank, *reinterpret_cast<float(*)[32]>(dp));
+      tmem_ld32(t_dpbank + 32, *reinterpret_cast<float(*)[32]>(dp + 32));
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
