@@ -3,6 +3,7 @@
 // cvt.rn.satfinite.e4m3x2.f32).  For every fp32 bit pattern u in (lo, hi] the
 // kernel compares the code of u with the code of u-1 and records each place
 // where it changes, so a short list describes the conversion of every pattern.
+#include "fp8.cuh"
 #include "internal.h"
 
 namespace fp4attn {
@@ -11,6 +12,7 @@ namespace {
 __device__ __forceinline__ uint32_t convert_one(int format, uint32_t bits) {
   const float x = __uint_as_float(bits);
   if (format == 0) return cvt_e2m1x8(x, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f) & 0xFu;
+  if (format == 2) return cvt_fp8x4<kFmtE5M2>(x, 0.f, 0.f, 0.f) & 0xFFu;
   return cvt_e4m3(x);
 }
 
@@ -164,7 +166,7 @@ extern "C" int fp4attn_debug_wait_timeout(int limit_us, void* stream) {
 
 extern "C" int fp4attn_debug_cvt_transitions(int format, uint32_t lo, uint32_t hi, uint32_t* pairs, int capacity,
                                              int* count, void* stream) {
-  if ((format != 0 && format != 1) || hi < lo || !pairs || !count || capacity <= 0) return FP4ATTN_ERR_INVALID_ARG;
+  if ((format < 0 || format > 2) || hi < lo || !pairs || !count || capacity <= 0) return FP4ATTN_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(count, 0, sizeof(int), s) != cudaSuccess) return FP4ATTN_ERR_CUDA;
   cvt_transitions_kernel<<<sm_count() * 8, 256, 0, s>>>(format, lo, hi, pairs, capacity, count);

@@ -350,8 +350,8 @@ int fp4attn_debug_dump_p_fp8pv(const fp4attn_nvfp4_t *q, const fp4attn_nvfp4_t *
                                int b, int h, int row0, int nrows, uint8_t *codes, int32_t *kshift,
                                float *o_f32, void *stream);
 
-/* Test support (no counterpart in the method): for format 0 (E2M1) or 1
- * (E4M3), converts every fp32 bit pattern u in [lo, hi] with the hardware
+/* Test support (no counterpart in the method): for format 0 (E2M1), 1
+ * (E4M3) or 2 (E5M2), converts every fp32 bit pattern u in [lo, hi] with the hardware
  * round-to-nearest-even saturating conversion the library uses, and records
  * into pairs[2i], pairs[2i+1] (device, capacity pairs) each pattern u > lo
  * whose code differs from that of u-1, plus the pair (lo, code(lo)); *count

@@ -1,5 +1,6 @@
-"""Exhaustive agreement of the hardware E2M1 / E4M3 conversions with the
-oracle's round-to-nearest-even encoders over every non-NaN fp32 bit pattern.
+"""Exhaustive agreement of the hardware E2M1 / E4M3 / E5M2 conversions with
+the oracle's round-to-nearest-even encoders over every non-NaN fp32 bit
+pattern (E5M2: the backward oracle's numpy encoder).
 The GPU reports where the code changes between neighbouring patterns; the
 oracle's change points come from bisection over its monotone encoder."""
 import struct
@@ -16,7 +17,11 @@ def _f(bits: int) -> float:
 
 
 def oracle_transitions(fmt, lo, hi):
-    enc = oracle.e2m1_encode if fmt == 0 else oracle.e4m3_encode
+    if fmt == 2:
+        import oracle.bwd as ob
+        enc = lambda y: int(ob.fp8_encode(y, ob.E5M2))
+    else:
+        enc = oracle.e2m1_encode if fmt == 0 else oracle.e4m3_encode
     code = lambda u: enc(_f(u))
     out = [(lo, code(lo))]
 
@@ -35,7 +40,7 @@ def oracle_transitions(fmt, lo, hi):
     return sorted(out)
 
 
-@pytest.mark.parametrize("fmt", [0, 1], ids=["e2m1", "e4m3"])
+@pytest.mark.parametrize("fmt", [0, 1, 2], ids=["e2m1", "e4m3", "e5m2"])
 @pytest.mark.parametrize("lo,hi", [(0x00000000, 0x7F800000), (0x80000000, 0xFF800000)], ids=["pos", "neg"])
 def test_hardware_conversion_matches_oracle(fmt, lo, hi):
     import blackwell_nvfp4_quantize_gb300 as fa
