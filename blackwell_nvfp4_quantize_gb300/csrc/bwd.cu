@@ -161,7 +161,7 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
 // exponent (returned) and 32 code bytes stored as two 16-byte chunks of a
 // 128-byte row under the 128-byte swizzle (chunk c of row r at c ^ (r % 8)).
 template <int FMT>
-__device__ __forceinline__ int mx_block_store(const float* x, uint8_t* row_base, int blk, int row) {
+__device__ __forceinline__ int mx_block_store(const float* x, uint32_t row_base, int blk, int row) {
   float amax = fabsf(x[0]);
 #pragma unroll
   for (int i = 1; i < 31; i += 2) amax = fmax3(amax, fabsf(x[i]), fabsf(x[i + 1]));
@@ -175,8 +175,8 @@ __device__ __forceinline__ int mx_block_store(const float* x, uint8_t* row_base,
 #pragma unroll
   for (int q = 0; q < 8; ++q) w[q] = cvt_fp8x4<FMT>(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
   const int c0 = 2 * blk, c1 = 2 * blk + 1;
-  *reinterpret_cast<uint4*>(row_base + ((c0 ^ (row & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
-  *reinterpret_cast<uint4*>(row_base + ((c1 ^ (row & 7)) * 16)) = make_uint4(w[4], w[5], w[6], w[7]);
+  sts_u4(row_base + ((c0 ^ (row & 7)) * 16), w[0], w[1], w[2], w[3]);
+  sts_u4(row_base + ((c1 ^ (row & 7)) * 16), w[4], w[5], w[6], w[7]);
   return e;
 }
 
@@ -436,15 +436,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       nl2_row = p.nl2[static_cast<size_t>(bh) * npad + row_id];
       delta_row = p.delta[static_cast<size_t>(bh) * npad + row_id];
     }
-    uint8_t* w1_row = smem + L::kW1 + row * 128;
-    uint8_t* w2_row = smem + L::kW2 + row * 128;
+    const uint32_t w1_row = smem_u32(smem + L::kW1 + row * 128);
+    const uint32_t w2_row = smem_u32(smem + L::kW2 + row * 128);
     // this thread's two scale bytes of its row's atom word
     const int at_off = (row & 31) * 16 + (row >> 5) * 4 + 2 * half;
     bool ok = true;
     for (int t = 0; t < nsteps; ++t) {
       const int s = t % kStages;
-      const float* st_nl2 = reinterpret_cast<const float*>(smem + L::stage_small(s) + L::kSsL) + col0;
-      const float* st_delta = reinterpret_cast<const float*>(smem + L::stage_small(s) + L::kSsDelta) + col0;
+      const uint32_t st_nl2 = smem_u32(smem + L::stage_small(s) + L::kSsL) + 4 * col0;
+      const uint32_t st_delta = smem_u32(smem + L::stage_small(s) + L::kSsDelta) + 4 * col0;
       const bool diag = streamed(t) == tile0;
       ok = mbar_wait(bar_s_full, t & 1, abort_flag, p.status, 40);
       // KV: this step's L and Delta are read from the stage, so the row
@@ -465,10 +465,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // P = 2^(c S - L), one FMA and ex2 per element; causal mask on the
       // diagonal tile (KV: query col < key row; Q: key col > query row)
 #pragma unroll
-      for (int i = 0; i < 64; i += 2) {
-        ffma2(pr[i], pr[i + 1], c, c, pr[i], pr[i + 1], KV ? st_nl2[i] : nl2_row, KV ? st_nl2[i + 1] : nl2_row);
-        pr[i] = ex2_approx(pr[i]);
-        pr[i + 1] = ex2_approx(pr[i + 1]);
+      for (int i = 0; i < 64; i += 4) {
+        const float4 l = KV ? lds_f4(st_nl2 + 4 * i) : make_float4(nl2_row, nl2_row, nl2_row, nl2_row);
+        ffma2(pr[i], pr[i + 1], c, c, pr[i], pr[i + 1], l.x, l.y);
+        ffma2(pr[i + 2], pr[i + 3], c, c, pr[i + 2], pr[i + 3], l.z, l.w);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) pr[i + u] = ex2_approx(pr[i + u]);
       }
       if (diag) {
 #pragma unroll
@@ -486,7 +488,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         const int e0 = mx_block_store<kFmtE4M3>(pr, w1_row, 2 * half, row);
         const int e1 = mx_block_store<kFmtE4M3>(pr + 32, w1_row, 2 * half + 1, row);
-        *reinterpret_cast<uint16_t*>(smem + L::kAtW1 + at_off) = static_cast<uint16_t>((e0 + 127) | ((e1 + 127) << 8));
+        sts_u16(smem_u32(smem + L::kAtW1 + at_off), static_cast<uint16_t>((e0 + 127) | ((e1 + 127) << 8)));
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_w1_full);
@@ -507,9 +509,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) mbar_arrive(bar_bank_free);
       // dS = P (dP - Delta), E5M2 codes blocked along this row's columns
 #pragma unroll
-      for (int i = 0; i < 64; i += 2) {
-        fsub2(dp[i], dp[i + 1], dp[i], dp[i + 1], KV ? st_delta[i] : delta_row, KV ? st_delta[i + 1] : delta_row);
+      for (int i = 0; i < 64; i += 4) {
+        const float4 dl = KV ? lds_f4(st_delta + 4 * i) : make_float4(delta_row, delta_row, delta_row, delta_row);
+        fsub2(dp[i], dp[i + 1], dp[i], dp[i + 1], dl.x, dl.y);
+        fsub2(dp[i + 2], dp[i + 3], dp[i + 2], dp[i + 3], dl.z, dl.w);
         fmul2(dp[i], dp[i + 1], pr[i], pr[i + 1], dp[i], dp[i + 1]);
+        fmul2(dp[i + 2], dp[i + 3], pr[i + 2], pr[i + 3], dp[i + 2], dp[i + 3]);
       }
       if (t > 0) {
         ok = mbar_wait(KV ? bar_w2_done : bar_w1_done, (t - 1) & 1, abort_flag, p.status, 43);
@@ -518,11 +523,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           break;
         }
       }
-      uint8_t* ds_row = KV ? w2_row : w1_row;
+      const uint32_t ds_row = KV ? w2_row : w1_row;
       const int e0 = mx_block_store<kFmtE5M2>(dp, ds_row, 2 * half, row);
       const int e1 = mx_block_store<kFmtE5M2>(dp + 32, ds_row, 2 * half + 1, row);
-      *reinterpret_cast<uint16_t*>(smem + (KV ? L::kAtW2 : L::kAtW1) + at_off) =
-          static_cast<uint16_t>((e0 + 127) | ((e1 + 127) << 8));
+      sts_u16(smem_u32(smem + (KV ? L::kAtW2 : L::kAtW1) + at_off), static_cast<uint16_t>((e0 + 127) | ((e1 + 127) << 8)));
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(KV ? bar_w2_full : bar_w1_full);
