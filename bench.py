@@ -69,7 +69,8 @@ TRAFFIC_RECORD = {"sources_sha": "84d51463d5b0f964", "shape": (1, 40, 32768, 128
 TRAFFIC_RECORD_CAUSAL = {"sources_sha": TRAFFIC_RECORD["sources_sha"], "shape": TRAFFIC_RECORD["shape"],
                          "bytes_per_launch": 279163392 + 293202432,
                          "note": "the same capture of the causal forward"}
-KERNEL_SOURCES = ["blackwell_nvfp4_quantize_gb300/csrc/fwd_directp.cu", "blackwell_nvfp4_quantize_gb300/csrc/ptx.cuh"]
+KERNEL_SOURCES = ["blackwell_nvfp4_quantize_gb300/csrc/fwd_directp.cu", "blackwell_nvfp4_quantize_gb300/csrc/ptx.cuh",
+                  "blackwell_nvfp4_quantize_gb300/csrc/fp8.cuh"]
 
 
 def sources_sha() -> str:

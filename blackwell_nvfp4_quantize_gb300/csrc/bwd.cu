@@ -23,9 +23,10 @@
 //       and the dV and dK accumulators stay in TMEM for the whole run.
 //   Q   one CTA per (128-query tile i, b*H+h), streaming the key tiles j <= i;
 //       rows are queries, one dQ accumulator.
-// Roles (320 threads): warps 0-7 row threads, two per row (= TMEM lane):
-// warps w and w+4 take columns 0-63 and 64-127 of the rows of lane quarter
-// w; warp 8 the TMA producer; warp 9 the MMA issuer and TMEM owner.  Every
+// Roles: kRowWarps row warps, kSplit per TMEM lane quarter: warp w takes
+// columns kCols (w / 4) .. + kCols - 1 of the rows of lane quarter w % 4
+// (row = TMEM lane); then the TMA producer warp and the MMA issuer warp
+// (also the TMEM owner).  Every
 // wait is bounded (the library's status word records where one gave up).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -40,7 +41,11 @@
 namespace fp4attn {
 namespace {
 
-constexpr int kRowWarps = 8;  // two per TMEM lane quarter: each thread takes half of its row's 128 columns
+// Row warps per TMEM lane quarter (kSplit) and the columns each row thread takes.
+constexpr int kSplit = 4;
+constexpr int kRowWarps = 4 * kSplit;
+constexpr int kCols = 128 / kSplit;  // one thread's columns of its row
+constexpr int kBlk = kCols / 32;     // its 32-column scale blocks
 constexpr int kBwdThreads = 32 * kRowWarps + 64;
 constexpr int kWarpLoad = kRowWarps, kWarpMma = kRowWarps + 1;
 constexpr uint32_t kBwdTmemCols = 512;
@@ -422,8 +427,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else {
     // ------------------------------------------------------------ row threads
     const int row = threadIdx.x & 127;  // == TMEM lane
-    const int half = warp >> 2;         // columns 64 half .. 64 half + 63
-    const int col0 = 64 * half;
+    const int part = warp >> 2;         // columns kCols part .. kCols part + kCols - 1
+    const int col0 = kCols * part;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t t_bank = tmem + lane_base + C::kBankS + col0;
     const uint32_t t_dpbank = tmem + lane_base + C::kBankDP + col0;
@@ -438,8 +443,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     const uint32_t w1_row = smem_u32(smem + L::kW1 + row * 128);
     const uint32_t w2_row = smem_u32(smem + L::kW2 + row * 128);
-    // this thread's two scale bytes of its row's atom word
-    const int at_off = (row & 31) * 16 + (row >> 5) * 4 + 2 * half;
+    // this thread's scale bytes in its row's atom word
+    const int at_off = (row & 31) * 16 + (row >> 5) * 4 + col0 / 32;
+    auto store_scales = [&](uint32_t atom, const int (&e)[kBlk]) {
+      if constexpr (kBlk == 2)
+        sts_u16(atom + at_off, static_cast<uint16_t>((e[0] + 127) | ((e[1] + 127) << 8)));
+      else
+        sts_u8(atom + at_off, static_cast<uint32_t>(e[0] + 127));
+    };
     bool ok = true;
     for (int t = 0; t < nsteps; ++t) {
       const int s = t % kStages;
@@ -455,9 +466,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       tc_fence_after();
-      float pr[64];
-      tmem_ld32(t_bank, *reinterpret_cast<float(*)[32]>(pr));
-      tmem_ld32(t_bank + 32, *reinterpret_cast<float(*)[32]>(pr + 32));
+      float pr[kCols];
+#pragma unroll
+      for (int b = 0; b < kBlk; ++b) tmem_ld32(t_bank + 32 * b, *reinterpret_cast<float(*)[32]>(pr + 32 * b));
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
@@ -465,7 +476,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // P = 2^(c S - L), one FMA and ex2 per element; causal mask on the
       // diagonal tile (KV: query col < key row; Q: key col > query row)
 #pragma unroll
-      for (int i = 0; i < 64; i += 4) {
+      for (int i = 0; i < kCols; i += 4) {
         const float4 l = KV ? lds_f4(st_nl2 + 4 * i) : make_float4(nl2_row, nl2_row, nl2_row, nl2_row);
         ffma2(pr[i], pr[i + 1], c, c, pr[i], pr[i + 1], l.x, l.y);
         ffma2(pr[i + 2], pr[i + 3], c, c, pr[i + 2], pr[i + 3], l.z, l.w);
@@ -474,7 +485,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (diag) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
+        for (int i = 0; i < kCols; ++i)
           if (KV ? (col0 + i < row) : (col0 + i > row)) pr[i] = 0.0f;
       }
       if constexpr (KV) {
@@ -486,9 +497,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             break;
           }
         }
-        const int e0 = mx_block_store<kFmtE4M3>(pr, w1_row, 2 * half, row);
-        const int e1 = mx_block_store<kFmtE4M3>(pr + 32, w1_row, 2 * half + 1, row);
-        sts_u16(smem_u32(smem + L::kAtW1 + at_off), static_cast<uint16_t>((e0 + 127) | ((e1 + 127) << 8)));
+        int e[kBlk];
+#pragma unroll
+        for (int b = 0; b < kBlk; ++b) e[b] = mx_block_store<kFmtE4M3>(pr + 32 * b, w1_row, col0 / 32 + b, row);
+        store_scales(smem_u32(smem + L::kAtW1), e);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_w1_full);
@@ -500,16 +512,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       tc_fence_after();
-      float dp[64];
-      tmem_ld32(t_dpbank, *reinterpret_cast<float(*)[32]>(dp));
-      tmem_ld32(t_dpbank + 32, *reinterpret_cast<float(*)[32]>(dp + 32));
+      float dp[kCols];
+#pragma unroll
+      for (int b = 0; b < kBlk; ++b) tmem_ld32(t_dpbank + 32 * b, *reinterpret_cast<float(*)[32]>(dp + 32 * b));
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_bank_free);
       // dS = P (dP - Delta), E5M2 codes blocked along this row's columns
 #pragma unroll
-      for (int i = 0; i < 64; i += 4) {
+      for (int i = 0; i < kCols; i += 4) {
         const float4 dl = KV ? lds_f4(st_delta + 4 * i) : make_float4(delta_row, delta_row, delta_row, delta_row);
         fsub2(dp[i], dp[i + 1], dp[i], dp[i + 1], dl.x, dl.y);
         fsub2(dp[i + 2], dp[i + 3], dp[i + 2], dp[i + 3], dl.z, dl.w);
@@ -524,9 +536,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       const uint32_t ds_row = KV ? w2_row : w1_row;
-      const int e0 = mx_block_store<kFmtE5M2>(dp, ds_row, 2 * half, row);
-      const int e1 = mx_block_store<kFmtE5M2>(dp + 32, ds_row, 2 * half + 1, row);
-      sts_u16(smem_u32(smem + (KV ? L::kAtW2 : L::kAtW1) + at_off), static_cast<uint16_t>((e0 + 127) | ((e1 + 127) << 8)));
+      int e[kBlk];
+#pragma unroll
+      for (int b = 0; b < kBlk; ++b) e[b] = mx_block_store<kFmtE5M2>(dp + 32 * b, ds_row, col0 / 32 + b, row);
+      store_scales(smem_u32(smem + (KV ? L::kAtW2 : L::kAtW1)), e);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(KV ? bar_w2_full : bar_w1_full);
@@ -538,22 +551,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (__all_sync(0xFFFFFFFFu, ok)) {
       tc_fence_after();
       const bool store = row_id < N;
-      // this thread writes channels D/2 half .. D/2 half + D/2 - 1 of its row
-      const size_t off = (static_cast<size_t>(bh) * N + (store ? row_id : 0)) * D + (D / 2) * half;
+      // this thread writes channels kOut part .. kOut part + kOut - 1 of its row
+      constexpr int kOut = D / kSplit;
+      const size_t off = (static_cast<size_t>(bh) * N + (store ? row_id : 0)) * D + kOut * part;
 #pragma unroll
       for (int acc = 0; acc < (KV ? 2 : 1); ++acc) {
         // KV: acc 0 = dV (unscaled), acc 1 = dK; Q: dQ
         const float scale = (KV && acc == 0) ? 1.0f : p.softmax_scale;
         float* dst = (acc == 0 ? p.out0 : p.out1) + off;
+        const uint32_t src = tmem + lane_base + (acc == 0 ? C::kAcc0 : C::kAcc1) + kOut * part;
+        if constexpr (kOut >= 32) {
 #pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc) {
-          float v[32];
-          tmem_ld32(tmem + lane_base + (acc == 0 ? C::kAcc0 : C::kAcc1) + (D / 2) * half + 32 * cc, v);
+          for (int cc = 0; cc < kOut / 32; ++cc) {
+            float v[32];
+            tmem_ld32(src + 32 * cc, v);
+            tmem_wait_ld();
+            if (store) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                reinterpret_cast<float4*>(dst + 32 * cc)[i] =
+                    make_float4(v[4 * i] * scale, v[4 * i + 1] * scale, v[4 * i + 2] * scale, v[4 * i + 3] * scale);
+            }
+          }
+        } else {
+          float v[16];
+          tmem_ld16(src, v);
           tmem_wait_ld();
           if (store) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              reinterpret_cast<float4*>(dst + 32 * cc)[i] =
+            for (int i = 0; i < 4; ++i)
+              reinterpret_cast<float4*>(dst)[i] =
                   make_float4(v[4 * i] * scale, v[4 * i + 1] * scale, v[4 * i + 2] * scale, v[4 * i + 3] * scale);
           }
         }

@@ -47,6 +47,7 @@
 #include <cmath>
 #include <mutex>
 
+#include "fp8.cuh"
 #include "internal.h"
 
 namespace fp4attn {
@@ -677,14 +678,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
       }
-      uint8_t* prow = sP + row * L::kKeyBytes;
+      const uint32_t prow = smem_u32(sP + row * L::kKeyBytes);
 #pragma unroll
       for (int u = 0; u < kWords / 4; ++u) {
         // 64-byte (E2M1) or 128-byte (E4M3) swizzle of the K-major P tile
         const int chunk = P8 ? (u ^ (row & 7)) : (u ^ ((row >> 1) & 3));
-        *reinterpret_cast<uint4*>(prow + chunk * 16) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+        sts_u4(prow + chunk * 16, w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
       }
-      *reinterpret_cast<uint32_t*>(sSFP + (row & 31) * 16 + (row >> 5) * 4) = sfword;
+      asm volatile("st.shared.u32 [%0], %1;" ::"r"(smem_u32(sSFP + (row & 31) * 16 + (row >> 5) * 4)), "r"(sfword) : "memory");
       if (dump_row) {
         const size_t rr = static_cast<size_t>(qrow - p.dump_row0);
         uint4* dst = reinterpret_cast<uint4*>(p.dump_codes + rr * (T * L::kKeyBytes) + j * L::kKeyBytes);
