@@ -62,12 +62,12 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic of one forward launch, from an ncu capture (see profiles/), and
 # the hash of the kernel sources it was taken on; reported only while the
 # sources are unchanged.
-TRAFFIC_RECORD = {"sources_sha": "84d51463d5b0f964", "shape": (1, 40, 32768, 128),
-                  "bytes_per_launch": 278163968 + 292270336,
+TRAFFIC_RECORD = {"sources_sha": "9bfce670efca4f95", "shape": (1, 40, 32768, 128),
+                  "bytes_per_launch": 278259968 + 291760896,
                   "note": "dram__bytes_read.sum + dram__bytes_write.sum of one launch on the 40-head "
                           "N=32768 D=128 workload (ncu capture of the same kernel sources)"}
 TRAFFIC_RECORD_CAUSAL = {"sources_sha": TRAFFIC_RECORD["sources_sha"], "shape": TRAFFIC_RECORD["shape"],
-                         "bytes_per_launch": 279163392 + 293202432,
+                         "bytes_per_launch": 278377216 + 293730304,
                          "note": "the same capture of the causal forward"}
 KERNEL_SOURCES = ["blackwell_nvfp4_quantize_gb300/csrc/fwd_directp.cu", "blackwell_nvfp4_quantize_gb300/csrc/ptx.cuh",
                   "blackwell_nvfp4_quantize_gb300/csrc/fp8.cuh"]
