@@ -89,3 +89,57 @@ def test_noalloc_needs_caller_outputs(fa):
         fa.fwd_directp_noalloc(_nv(fa), _nv(fa), _mx(fa), None, torch.zeros((B, H, N)))
     with pytest.raises(ValueError, match="caller-provided"):
         fa.fwd_directp_noalloc(_nv(fa), _nv(fa), _mx(fa), torch.zeros((B, H, N, D), dtype=torch.bfloat16), None)
+
+
+def _fp8(fa, layout, fmt, shape=SHAPE, payload_n=None):
+    B, H, N, D = shape
+    pb, sb = (fa.mxfp8_rows_bytes if layout == "rows" else fa.mxfp8_v_bytes)(B, H, N, D)
+    return fa.FP8Tensor(torch.zeros(payload_n or pb, dtype=torch.uint8), torch.zeros(sb, dtype=torch.uint8),
+                        tuple(shape), layout, fmt)
+
+
+def _bwd_args(fa, **over):
+    B, H, N, D = SHAPE
+    npad = (N + 127) // 128 * 128
+    args = dict(q_saved=_nv(fa), k_saved=_nv(fa), v_rows=_fp8(fa, "rows", fa.FP8_E4M3),
+                do_rows=_fp8(fa, "rows", fa.FP8_E5M2), do_t=_fp8(fa, "t", fa.FP8_E5M2),
+                q_t=_fp8(fa, "t", fa.FP8_E4M3), k_t=_fp8(fa, "t", fa.FP8_E4M3),
+                nl2=torch.zeros(B * H * npad), delta=torch.zeros(B * H * npad))
+    args.update(over)
+    return args
+
+
+def test_backward_operands_checked(fa):
+    # well-formed CPU operands stop at the device check
+    with pytest.raises(ValueError, match="CUDA"):
+        fa.bwd_directp_causal(**_bwd_args(fa))
+    # a format or layout swapped, a short payload, a short workspace
+    with pytest.raises(ValueError):
+        fa.bwd_directp_causal(**_bwd_args(fa, do_rows=_fp8(fa, "rows", fa.FP8_E4M3)))
+    with pytest.raises(ValueError):
+        fa.bwd_directp_causal(**_bwd_args(fa, q_t=_fp8(fa, "rows", fa.FP8_E4M3)))
+    with pytest.raises(ValueError):
+        fa.bwd_directp_causal(**_bwd_args(fa, k_t=_fp8(fa, "t", fa.FP8_E4M3, payload_n=10)))
+    with pytest.raises(ValueError):
+        fa.bwd_directp_causal(**_bwd_args(fa, nl2=torch.zeros(5)))
+    with pytest.raises(ValueError):
+        fa.bwd_directp_causal(**_bwd_args(fa, delta=torch.zeros(SHAPE[0] * SHAPE[1] * 256, dtype=torch.float64)))
+    with pytest.raises(ValueError):
+        fa.bwd_directp_causal(**_bwd_args(fa, k_saved=_nv(fa, shape=(1, 2, 256, 64))))
+    # preallocated gradients of the wrong size or dtype
+    with pytest.raises(ValueError):
+        fa.bwd_directp_causal(**_bwd_args(fa), dq=torch.zeros(3))
+    with pytest.raises(ValueError):
+        fa.bwd_directp_causal(**_bwd_args(fa), dv=torch.zeros(SHAPE, dtype=torch.bfloat16))
+
+
+def test_backward_quantizer_and_prep_inputs(fa):
+    x = torch.zeros(SHAPE, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.quant_mxfp8_rows(x, fa.FP8_E5M2)  # CPU input
+    with pytest.raises(ValueError):
+        fa.quant_mxfp8_t(x.float(), fa.FP8_E4M3)  # not bf16
+    with pytest.raises(ValueError):
+        fa.empty_fp8(SHAPE, "cols", fa.FP8_E4M3, "cpu")
+    with pytest.raises(ValueError):
+        fa.bwd_prep(x, x, torch.zeros(SHAPE[:3]))  # CPU inputs

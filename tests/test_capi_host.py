@@ -153,3 +153,48 @@ def test_noalloc_debug_argument_errors(L):
     assert L.fp4attn_debug_noalloc_timeout(ctypes.c_void_p(0x1000), 0, 100, None) == fa.FP4ATTN_ERR_INVALID_ARG
     assert L.fp4attn_debug_noalloc_timeout(ctypes.c_void_p(0x1000), 16, 0, None) == fa.FP4ATTN_ERR_INVALID_ARG
     assert L.fp4attn_debug_status_word_exists(None) == fa.FP4ATTN_ERR_INVALID_ARG
+
+
+def test_backward_argument_errors_without_gpu(L):
+    import blackwell_nvfp4_quantize_gb300 as fa
+
+    n = None
+    good = ctypes.c_void_p(0x6000)
+    # FP8 operand quantizers: null / misaligned pointers, bad format, bad D
+    for fn in (L.fp4attn_quant_mxfp8_t, L.fp4attn_quant_mxfp8_rows):
+        assert fn(n, good, good, 0, 1, 1, 128, 64, n) == fa.FP4ATTN_ERR_INVALID_ARG
+        assert fn(good, ctypes.c_void_p(0x6004), good, 0, 1, 1, 128, 64, n) == fa.FP4ATTN_ERR_INVALID_ARG
+        assert fn(good, good, good, 2, 1, 1, 128, 64, n) == fa.FP4ATTN_ERR_INVALID_ARG
+        assert fn(good, good, good, -1, 1, 1, 128, 64, n) == fa.FP4ATTN_ERR_INVALID_ARG
+        assert fn(good, good, good, 1, 1, 1, 128, 96, n) == fa.FP4ATTN_ERR_UNSUPPORTED
+    # sizes
+    assert fa.mxfp8_rows_bytes(1, 40, 32768, 128) == (40 * 32768 * 128, 40 * 256 * 512)
+    assert fa.mxfp8_rows_bytes(2, 3, 77, 64) == (6 * 77 * 64, 6 * 512)
+    assert fa.bwd_workspace_bytes(2, 3, 77, 64) == (6 * 128 * 4, 6 * 128 * 4)
+    with pytest.raises(fa.Fp4AttnError):
+        fa.bwd_workspace_bytes(1, 1, 0, 64)
+    # prep
+    assert L.fp4attn_bwd_prep(good, good, good, good, n, 1, 1, 128, 64, n) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert L.fp4attn_bwd_prep(good, good, ctypes.c_void_p(0x6002), good, good, 1, 1, 128, 64, n) == \
+        fa.FP4ATTN_ERR_INVALID_ARG
+    assert L.fp4attn_bwd_prep(good, good, good, good, good, 1, 1, 128, 80, n) == fa.FP4ATTN_ERR_UNSUPPORTED
+    # the backward: every operand struct, workspace and output is checked first
+    q = fa._NVFP4(0x1000, 0x2000, 0x3000)
+    f8 = fa._MXFP4(0x4000, 0x5000)
+    f8_bad = fa._MXFP4(0x4000, 0)
+    ops = [ctypes.byref(f8)] * 5
+
+    def call(q1=q, k1=q, fp8=ops, nl2=good, delta=good, dq=good, dk=good, dv=good, D=64, scale=0.1):
+        return L.fp4attn_bwd_directp_causal(ctypes.byref(q1), ctypes.byref(k1), *fp8, nl2, delta, dq, dk, dv, 1, 1,
+                                            128, D, ctypes.c_float(scale), n)
+
+    assert call(k1=fa._NVFP4(0x1000, 0x2000, 0)) == fa.FP4ATTN_ERR_INVALID_ARG
+    for i in range(5):
+        bad_ops = list(ops)
+        bad_ops[i] = ctypes.byref(f8_bad)
+        assert call(fp8=bad_ops) == fa.FP4ATTN_ERR_INVALID_ARG, i
+    assert call(nl2=n) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert call(dv=ctypes.c_void_p(0x6008)) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert call(scale=-1.0) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert call(D=32) == fa.FP4ATTN_ERR_UNSUPPORTED
