@@ -154,14 +154,6 @@ struct BwdParams {
   float softmax_scale;
 };
 
-// 128 fp32 values of this thread's TMEM lane, four 32-column loads.
-__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
-  tmem_ld32(taddr + 0, *reinterpret_cast<float(*)[32]>(v + 0));
-  tmem_ld32(taddr + 32, *reinterpret_cast<float(*)[32]>(v + 32));
-  tmem_ld32(taddr + 64, *reinterpret_cast<float(*)[32]>(v + 64));
-  tmem_ld32(taddr + 96, *reinterpret_cast<float(*)[32]>(v + 96));
-}
-
 // One 32-element block of fp32 values -> MX FP8 codes: the block's scale
 // exponent (returned) and 32 code bytes stored as two 16-byte chunks of a
 // 128-byte row under the 128-byte swizzle (chunk c of row r at c ^ (r % 8)).
@@ -399,8 +391,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     };
     // Software pipeline: each product is issued as soon as its bank and
     // operands are ready, ahead of the current step's last products.
-    //   one bank,  KV step t: dV(t) [P~ is written early], S(t+1) [after the
-    //              dP(t) pull], dK(t), dP(t+1) [after the S(t+1) pull]
+    //   one bank,  KV step t: S(t+1) [after the dP(t) pull; ahead of dV(t),
+    //              which is only needed before the next P~ is written],
+    //              dV(t), dK(t), dP(t+1) [after the S(t+1) pull]
     //   two banks, KV step t: S(t+1) [after the S(t) pull], dV(t), dP(t+1)
     //              [after the dP(t) pull], dK(t)
     //   two banks, Q  step t: S(t+1), dP(t+1), dQ(t) [dS~ is written last]
@@ -414,8 +407,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!(ok = KV ? issue_w2(t) : issue_w1(t))) break;
         tc_commit_warp(bar_empty + (t % kStages));
       } else {
-        if (!(ok = issue_w1(t))) break;
         if (more && !(ok = issue_s(t + 1))) break;
+        if (!(ok = issue_w1(t))) break;
         if (!(ok = issue_w2(t))) break;
         tc_commit_warp(bar_empty + (t % kStages));
         if (more && !(ok = issue_dp(t + 1))) break;
