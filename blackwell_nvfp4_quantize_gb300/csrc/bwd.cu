@@ -60,15 +60,21 @@ __host__ __device__ constexpr uint32_t idesc_mxf8_fmt(uint32_t M, uint32_t N, ui
 }
 
 // Shared-memory plan.  "Stationary" operands are loaded once per CTA, the
-// others once per streamed tile into a ring of stages.
+// others once per streamed tile, in two rings:
 //   A4  NVFP4 tile of the stationary side (KV: K^, Q: Q^), 128 x D/2 bytes
 //   A8  MXFP8 rows of the stationary side (KV: E4M3 V, Q: E5M2 dO), 128 x D
 //   W1  the first tile the row threads write (KV: E4M3 P~^T, Q: E5M2 dS~),
 //       128 x 128 bytes; W2 (KV only) the second (E5M2 dS~^T)
-//   per stage: B4 (KV: Q^, Q: K^), B8 (KV: E5M2 dO rows, Q: E4M3 V rows),
-//       T1 (sequence-blocked, transposed: KV: E5M2 dO^T, Q: E4M3 K^T), T2
-//       (KV only: E4M3 Q^T), and (KV only) 128 fp32 L and 128 fp32 Delta
-// 128-byte-swizzled tiles start on 1024-byte boundaries.
+//   ring A (operands of S and dP, needed first in a step): B4 (KV: Q^, Q:
+//       K^) with its scale atoms, B8 (KV: E5M2 dO rows, Q: E4M3 V rows) with
+//       its atom, and (KV only) the tile's 128 fp32 -L and 128 fp32 Delta
+//   ring B (operands of the step's last products): T1 (sequence-blocked,
+//       transposed: KV: E5M2 dO^T, Q: E4M3 K^T), T2 (KV only: E4M3 Q^T),
+//       with their atoms
+// Ring A gets the deeper ring: its slot is free as soon as the step's S and
+// dP products are complete and its -L / Delta read, well before the step's
+// last products release ring B.  128-byte-swizzled tiles start on 1024-byte
+// boundaries.
 template <int D, bool KV>
 struct BwdLayout {
   static constexpr int kT4 = 128 * D / 2;
@@ -79,37 +85,47 @@ struct BwdLayout {
   static constexpr int kA8 = kA4 + kT4;
   static constexpr int kW1 = kA8 + kT8;
   static constexpr int kW2 = kW1 + kTW;
-  static constexpr int kStage0 = kW2 + (KV ? kTW : 0);
-  static constexpr int kStageBig = kT4 + kT8 + kT8 + (KV ? kT8 : 0);
-  static constexpr int kStageSmall = kSf4 + 512 + 512 + (KV ? 512 + 512 + 512 : 0);
+  static constexpr int kRing0 = kW2 + (KV ? kTW : 0);
+  static constexpr int kBigA = kT4 + kT8;                    // B4, B8
+  static constexpr int kBigB = kT8 + (KV ? kT8 : 0);         // T1, T2
+  static constexpr int kSmallA = kSf4 + 512 + (KV ? 1024 : 0);  // B4 scales, B8 atom, -L, Delta
+  static constexpr int kSmallB = 512 + (KV ? 512 : 0);          // T1 atom, T2 atom
   static constexpr int kFixedSmall = kSf4 + 512 + 512 + (KV ? 512 : 0);
-  static constexpr int kNumBarsMax = 1 + 2 * 4 + 10;
+  static constexpr int kNumBarsMax = 1 + 2 * 8 + 10;
   static constexpr int kBudget = 225 * 1024;
-  static constexpr int kFit = (kBudget - kStage0 - kFixedSmall - kNumBarsMax * 8 - 64) / (kStageBig + kStageSmall);
-  static constexpr int kStages = kFit < 4 ? kFit : 4;
-  // per-stage tiles
-  static constexpr int kB4 = 0, kB8 = kT4, kT1 = kT4 + kT8, kT2 = kT4 + 2 * kT8;
-  __host__ __device__ static constexpr int stage_big(int s) { return kStage0 + s * kStageBig; }
+  static constexpr int kAvail = kBudget - kRing0 - kFixedSmall - kNumBarsMax * 8 - 64;
+  static constexpr int kFitA = (kAvail - 2 * (kBigB + kSmallB)) / (kBigA + kSmallA);
+  static constexpr int kStagesA = kFitA < 4 ? kFitA : 4;
+  static constexpr int kFitB = (kAvail - kStagesA * (kBigA + kSmallA)) / (kBigB + kSmallB);
+  static constexpr int kStagesB = kFitB < 4 ? kFitB : 4;
+  // ring tiles
+  static constexpr int kB4 = 0, kB8 = kT4;  // within an A slot
+  static constexpr int kT1 = 0, kT2 = kT8;  // within a B slot
+  static constexpr int kRingB0 = kRing0 + kStagesA * kBigA;
+  __host__ __device__ static constexpr int big_a(int s) { return kRing0 + s * kBigA; }
+  __host__ __device__ static constexpr int big_b(int s) { return kRingB0 + s * kBigB; }
   // small buffers after every big tile
-  static constexpr int kSmall = kStage0 + kStages * kStageBig;
+  static constexpr int kSmall = kRingB0 + kStagesB * kBigB;
   static constexpr int kSfA4 = kSmall;
   static constexpr int kAtA8 = kSfA4 + kSf4;
   static constexpr int kAtW1 = kAtA8 + 512;
   static constexpr int kAtW2 = kAtW1 + 512;  // KV only
-  static constexpr int kStageSmall0 = kAtW1 + 512 + (KV ? 512 : 0);
-  // per-stage small: B4 scales, B8 atom, T1 atom, T2 atom, L, Delta
-  static constexpr int kSsB4 = 0, kSsB8 = kSf4, kSsT1 = kSf4 + 512, kSsT2 = kSf4 + 1024, kSsL = kSf4 + 1536,
-                       kSsDelta = kSf4 + 2048;
-  __host__ __device__ static constexpr int stage_small(int s) { return kStageSmall0 + s * kStageSmall; }
-  static constexpr int kBars = kStageSmall0 + kStages * kStageSmall;
-  static constexpr int kNumBars = 1 + 2 * kStages + 10;
+  static constexpr int kSmallA0 = kAtW1 + 512 + (KV ? 512 : 0);
+  static constexpr int kSsB4 = 0, kSsB8 = kSf4, kSsL = kSf4 + 512, kSsDelta = kSf4 + 1024;  // in an A slot
+  static constexpr int kSsT1 = 0, kSsT2 = 512;                                              // in a B slot
+  static constexpr int kSmallB0 = kSmallA0 + kStagesA * kSmallA;
+  __host__ __device__ static constexpr int small_a(int s) { return kSmallA0 + s * kSmallA; }
+  __host__ __device__ static constexpr int small_b(int s) { return kSmallB0 + s * kSmallB; }
+  static constexpr int kBars = kSmallB0 + kStagesB * kSmallB;
+  static constexpr int kNumBars = 1 + 2 * kStagesA + 2 * kStagesB + 10;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = (kBytes + 1024 > 120 * 1024) ? kBytes + 1024 : 120 * 1024;
-  static_assert(kStages >= 2, "the ring needs two stages");
+  static_assert(kStagesA >= 2 && kStagesB >= 2, "each ring needs two slots");
+  static_assert(kNumBars <= kNumBarsMax, "barrier space");
   static_assert(kAlloc <= 227 * 1024, "shared memory of one CTA");
-  static_assert(kA8 % 1024 == 0 && kW1 % 1024 == 0 && kStage0 % 1024 == 0 && kStageBig % 1024 == 0 &&
-                    kB8 % 1024 == 0 && kT1 % 1024 == 0 && kT2 % 1024 == 0,
+  static_assert(kA8 % 1024 == 0 && kW1 % 1024 == 0 && kRing0 % 1024 == 0 && kBigA % 1024 == 0 &&
+                    kBigB % 1024 == 0 && kB8 % 1024 == 0 && kT2 % 1024 == 0 && kRingB0 % 1024 == 0,
                 "tiles keep 1024-B alignment");
 };
 
@@ -185,14 +201,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                const BwdParams p) {
   using L = BwdLayout<D, KV>;
   using C = BwdCols<D, KV>;
-  constexpr int kStages = L::kStages;
+  constexpr int kSA = L::kStagesA, kSB = L::kStagesB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
   uint64_t* bar_fixed = bars;
-  uint64_t* bar_full = bars + 1;
-  uint64_t* bar_empty = bars + 1 + kStages;
-  uint64_t* bar_s_full = bars + 1 + 2 * kStages;  // S (S^T) is in the bank
+  uint64_t* bar_full_a = bars + 1;                 // [kSA] ring A slot landed
+  uint64_t* bar_empty_a = bar_full_a + kSA;        // [kSA] ring A slot free
+  uint64_t* bar_full_b = bar_empty_a + kSA;        // [kSB] ring B slot landed
+  uint64_t* bar_empty_b = bar_full_b + kSB;        // [kSB] ring B slot free
+  uint64_t* bar_s_full = bar_empty_b + kSB;        // S (S^T) is in the bank
   uint64_t* bar_pulled = bar_s_full + 1;          // the row threads hold S (one bank: it may take dP)
   uint64_t* bar_dp_full = bar_s_full + 2;         // dP (dP^T) is in its bank
   uint64_t* bar_bank_free = bar_s_full + 3;       // dP pulled (one bank: it may take the next S)
@@ -217,9 +235,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar_fixed, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar_full + s, 1);
-      mbar_init(bar_empty + s, 1);
+    for (int s = 0; s < kSA; ++s) {
+      mbar_init(bar_full_a + s, 1);
+      mbar_init(bar_empty_a + s, 1);
+    }
+    for (int s = 0; s < kSB; ++s) {
+      mbar_init(bar_full_b + s, 1);
+      mbar_init(bar_empty_b + s, 1);
     }
     mbar_init(bar_s_full, 1);
     mbar_init(bar_pulled, kRowWarps);
@@ -264,39 +286,58 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     int issued = 0;
     for (int t = 0; t < nsteps; ++t) {
-      const int s = t % kStages;
-      if (t >= kStages) {
-        const bool ok = mbar_wait(bar_empty + s, ((t / kStages) - 1) & 1, abort_flag, p.status, 30);
+      const int sa = t % kSA, sb = t % kSB;
+      if (t >= kSA) {
+        const bool ok = mbar_wait(bar_empty_a + sa, ((t / kSA) - 1) & 1, abort_flag, p.status, 30);
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
       }
+      const int u = streamed(t);
+      const size_t at = (static_cast<size_t>(bh) * T + u) * 512;
       if (leader) {
-        const int u = streamed(t);
-        uint8_t* big = smem + L::stage_big(s);
-        uint8_t* small = smem + L::stage_small(s);
-        const size_t at = (static_cast<size_t>(bh) * T + u) * 512;
-        constexpr uint32_t kTx =
-            L::kT4 + 2 * L::kT8 + L::kSf4 + 1024 + (KV ? L::kT8 + 512 + 512 + 512 : 0);
-        mbar_arrive_expect_tx(bar_full + s, kTx);
-        tma_load_3d(big + L::kB4, &tm_b4, bar_full + s, 0, u * 128, bh);
-        tma_load_3d(big + L::kB8, &tm_b8, bar_full + s, 0, u * 128, bh);
-        tma_load_2d(big + L::kT1, &tm_t1, bar_full + s, u * 128, bh * D);
-        bulk_load(small + L::kSsB4, p.sf_b4 + (static_cast<size_t>(bh) * T + u) * sf4_bytes, L::kSf4, bar_full + s);
-        bulk_load(small + L::kSsB8, p.at_b8 + at, 512, bar_full + s);
-        bulk_load(small + L::kSsT1, p.at_t1 + at, 512, bar_full + s);
+        uint8_t* big = smem + L::big_a(sa);
+        uint8_t* small = smem + L::small_a(sa);
+        constexpr uint32_t kTxA = L::kT4 + L::kT8 + L::kSf4 + 512 + (KV ? 1024 : 0);
+        mbar_arrive_expect_tx(bar_full_a + sa, kTxA);
+        tma_load_3d(big + L::kB4, &tm_b4, bar_full_a + sa, 0, u * 128, bh);
+        tma_load_3d(big + L::kB8, &tm_b8, bar_full_a + sa, 0, u * 128, bh);
+        bulk_load(small + L::kSsB4, p.sf_b4 + (static_cast<size_t>(bh) * T + u) * sf4_bytes, L::kSf4,
+                  bar_full_a + sa);
+        bulk_load(small + L::kSsB8, p.at_b8 + at, 512, bar_full_a + sa);
         if (KV) {
-          tma_load_2d(big + L::kT2, &tm_t2, bar_full + s, u * 128, bh * D);
-          bulk_load(small + L::kSsT2, p.at_t2 + at, 512, bar_full + s);
           const size_t lo = static_cast<size_t>(bh) * npad + static_cast<size_t>(u) * 128;
-          bulk_load(small + L::kSsL, p.nl2 + lo, 512, bar_full + s);
-          bulk_load(small + L::kSsDelta, p.delta + lo, 512, bar_full + s);
+          bulk_load(small + L::kSsL, p.nl2 + lo, 512, bar_full_a + sa);
+          bulk_load(small + L::kSsDelta, p.delta + lo, 512, bar_full_a + sa);
+        }
+      }
+      __syncwarp();
+      if (t >= kSB) {
+        const bool ok = mbar_wait(bar_empty_b + sb, ((t / kSB) - 1) & 1, abort_flag, p.status, 29);
+        if (!__all_sync(0xFFFFFFFFu, ok)) {
+          issued = -(t + 1);  // ring A of step t was issued, ring B was not
+          break;
+        }
+      }
+      if (leader) {
+        uint8_t* big = smem + L::big_b(sb);
+        uint8_t* small = smem + L::small_b(sb);
+        constexpr uint32_t kTxB = L::kT8 + 512 + (KV ? L::kT8 + 512 : 0);
+        mbar_arrive_expect_tx(bar_full_b + sb, kTxB);
+        tma_load_2d(big + L::kT1, &tm_t1, bar_full_b + sb, u * 128, bh * D);
+        bulk_load(small + L::kSsT1, p.at_t1 + at, 512, bar_full_b + sb);
+        if (KV) {
+          tma_load_2d(big + L::kT2, &tm_t2, bar_full_b + sb, u * 128, bh * D);
+          bulk_load(small + L::kSsT2, p.at_t2 + at, 512, bar_full_b + sb);
         }
       }
       issued = t + 1;
       __syncwarp();
     }
     // no copy into this CTA's shared memory may be in flight when it leaves
-    for (int t = issued - kStages < 0 ? 0 : issued - kStages; t < issued; ++t)
-      mbar_wait_drain(bar_full + (t % kStages), (t / kStages) & 1, abort_flag, p.status, 31);
+    const int issued_a = issued < 0 ? -issued : issued, issued_b = issued < 0 ? -issued - 1 : issued;
+    for (int t = issued_a - kSA < 0 ? 0 : issued_a - kSA; t < issued_a; ++t)
+      mbar_wait_drain(bar_full_a + (t % kSA), (t / kSA) & 1, abort_flag, p.status, 31);
+    for (int t = issued_b - kSB < 0 ? 0 : issued_b - kSB; t < issued_b; ++t)
+      mbar_wait_drain(bar_full_b + (t % kSB), (t / kSB) & 1, abort_flag, p.status, 28);
     mbar_wait_drain(bar_fixed, 0, abort_flag, p.status, 32);
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
@@ -324,17 +365,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     // S = A4 B4^T of step t into the bank (its stage has landed, the bank is free)
     auto issue_s = [&](int t) {
-      const int s = t % kStages;
-      if (!wait(bar_full + s, (t / kStages) & 1, 34)) return false;
+      const int s = t % kSA;
+      if (!wait(bar_full_a + s, (t / kSA) & 1, 34)) return false;
       // the S bank is free once the row threads hold the previous S (two
       // banks) or the previous dP (one bank)
       if (t > 0 && !wait(C::kTwoBanks ? bar_pulled : bar_bank_free, (t - 1) & 1, 35)) return false;
       tc_fence_after();
-      uint8_t* small = smem + L::stage_small(s);
+      uint8_t* small = smem + L::small_a(s);
 #pragma unroll
       for (int a = 0; a < D / 64; ++a)
         tc_cp_sf_atom_warp(tmem + C::kSfB4 + 4 * a, smem_u32(small + L::kSsB4 + a * 512));
-      const uint64_t b4 = smem_desc(smem_u32(smem + L::stage_big(s) + L::kB4), 16, kSbo4, kSw4);
+      const uint64_t b4 = smem_desc(smem_u32(smem + L::big_a(s) + L::kB4), 16, kSbo4, kSw4);
 #pragma unroll
       for (int ks = 0; ks < D / 64; ++ks)
         mma_nvf4_warp(bank_s, a4 + 2 * ks, b4 + 2 * ks, idesc_s, tmem + C::kSfA4 + 4 * ks, tmem + C::kSfB4 + 4 * ks,
@@ -345,27 +386,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // dP = A8 B8^T of step t: into its own bank once the previous dP is
     // pulled (two banks), or into the S bank once the row threads hold S
     auto issue_dp = [&](int t) {
-      const int s = t % kStages;
+      const int s = t % kSA;
       if (C::kTwoBanks ? (t > 0 && !wait(bar_bank_free, (t - 1) & 1, 36)) : !wait(bar_pulled, t & 1, 36))
         return false;
       tc_fence_after();
-      tc_cp_sf_atom_warp(tmem + C::kSfB8, smem_u32(smem + L::stage_small(s) + L::kSsB8));
-      const uint64_t b8 = smem_desc(smem_u32(smem + L::stage_big(s) + L::kB8), 16, kSbo8, kSw8);
+      tc_cp_sf_atom_warp(tmem + C::kSfB8, smem_u32(smem + L::small_a(s) + L::kSsB8));
+      const uint64_t b8 = smem_desc(smem_u32(smem + L::big_a(s) + L::kB8), 16, kSbo8, kSw8);
 #pragma unroll
       for (int ks = 0; ks < D / 32; ++ks)
         mma_mxf8_warp(bank_dp, a8 + 2 * ks, b8 + 2 * ks, idesc_mxf8_fmt(128, 128, kFmtA8, kFmtB8, ks, ks),
                       tmem + C::kSfA8, tmem + C::kSfB8, ks > 0);
       tc_commit_warp(bar_dp_full);
+      // Q: ring A of step t is free once S(t) and dP(t) are complete (the row
+      // threads read nothing from it)
+      if (!KV) tc_commit_warp(bar_empty_a + s);
       return true;
     };
     // acc0 += W1 T1^T  (KV: dV += P~^T dO, Q: dQ += dS~ K)
     auto issue_w1 = [&](int t) {
-      const int s = t % kStages;
+      const int s = t % kSB;
+      if (!wait(bar_full_b + s, (t / kSB) & 1, 48)) return false;
       if (!wait(bar_w1_full, t & 1, 37)) return false;
       tc_fence_after();
       tc_cp_sf_atom_warp(tmem + C::kSfW1, smem_u32(smem + L::kAtW1));
-      tc_cp_sf_atom_warp(tmem + C::kSfT1, smem_u32(smem + L::stage_small(s) + L::kSsT1));
-      const uint64_t t1 = smem_desc(smem_u32(smem + L::stage_big(s) + L::kT1), 16, 1024, 2u);
+      tc_cp_sf_atom_warp(tmem + C::kSfT1, smem_u32(smem + L::small_b(s) + L::kSsT1));
+      const uint64_t t1 = smem_desc(smem_u32(smem + L::big_b(s) + L::kT1), 16, 1024, 2u);
       constexpr uint32_t kFmtW1 = KV ? kFmtE4M3 : kFmtE5M2, kFmtT1 = KV ? kFmtE5M2 : kFmtE4M3;
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
@@ -376,12 +421,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     };
     // KV: acc1 += W2 T2^T  (dK += dS~^T Q)
     auto issue_w2 = [&](int t) {
-      const int s = t % kStages;
+      const int s = t % kSB;
       if (!wait(bar_w2_full, t & 1, 38)) return false;
+      // KV: the row threads are done with the step's -L and Delta: ring A's
+      // slot is free (S and dP of the step are complete: dP has been pulled)
+      if (KV && lane == 0) mbar_arrive(bar_empty_a + (t % kSA));
       tc_fence_after();
       tc_cp_sf_atom_warp(tmem + C::kSfW2, smem_u32(smem + L::kAtW2));
-      tc_cp_sf_atom_warp(tmem + C::kSfT2, smem_u32(smem + L::stage_small(s) + L::kSsT2));
-      const uint64_t t2 = smem_desc(smem_u32(smem + L::stage_big(s) + L::kT2), 16, 1024, 2u);
+      tc_cp_sf_atom_warp(tmem + C::kSfT2, smem_u32(smem + L::small_b(s) + L::kSsT2));
+      const uint64_t t2 = smem_desc(smem_u32(smem + L::big_b(s) + L::kT2), 16, 1024, 2u);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
         mma_mxf8_warp(tmem + C::kAcc1, w2 + 2 * ks, t2 + 2 * ks, idesc_mxf8_fmt(128, D, kFmtE5M2, kFmtE4M3, ks, ks),
@@ -405,12 +453,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (KV && !(ok = issue_w1(t))) break;
         if (more && !(ok = issue_dp(t + 1))) break;
         if (!(ok = KV ? issue_w2(t) : issue_w1(t))) break;
-        tc_commit_warp(bar_empty + (t % kStages));
+        tc_commit_warp(bar_empty_b + (t % kSB));
       } else {
         if (more && !(ok = issue_s(t + 1))) break;
         if (!(ok = issue_w1(t))) break;
         if (!(ok = issue_w2(t))) break;
-        tc_commit_warp(bar_empty + (t % kStages));
+        tc_commit_warp(bar_empty_b + (t % kSB));
         if (more && !(ok = issue_dp(t + 1))) break;
       }
     }
@@ -446,14 +494,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     };
     bool ok = true;
     for (int t = 0; t < nsteps; ++t) {
-      const int s = t % kStages;
-      const uint32_t st_nl2 = smem_u32(smem + L::stage_small(s) + L::kSsL) + 4 * col0;
-      const uint32_t st_delta = smem_u32(smem + L::stage_small(s) + L::kSsDelta) + 4 * col0;
+      const int s = t % kSA;
+      const uint32_t st_nl2 = smem_u32(smem + L::small_a(s) + L::kSsL) + 4 * col0;
+      const uint32_t st_delta = smem_u32(smem + L::small_a(s) + L::kSsDelta) + 4 * col0;
       const bool diag = streamed(t) == tile0;
       ok = mbar_wait(bar_s_full, t & 1, abort_flag, p.status, 40);
       // KV: this step's L and Delta are read from the stage, so the row
       // threads observe the stage's own TMA barrier as well
-      if (KV && ok) ok = mbar_wait(bar_full + s, (t / kStages) & 1, abort_flag, p.status, 46);
+      if (KV && ok) ok = mbar_wait(bar_full_a + s, (t / kSA) & 1, abort_flag, p.status, 46);
       if (!__all_sync(0xFFFFFFFFu, ok)) {
         ok = false;
         break;
