@@ -548,53 +548,29 @@ def run_ours(args, w):
     if fa.device_status() != fa.FP4ATTN_OK:
         raise RuntimeError("device-side wait timed out in the timed region")
 
-    # End to end through the public API with host buffers (pinned): every step
-    # uploads its Q, K, V and downloads its O and LSE inside the timed region.
-    # Steps run the way a serving loop runs them back to back: step i+1's
-    # upload and step i-1's download overlap step i's kernels (an upload and a
-    # download stream beside the compute stream, two device slots for inputs
-    # and outputs).
+    # End to end through the C ABI with host buffers (pinned): one
+    # fp4attn_fwd_host_batch call runs the K steps, each uploading its Q, K, V
+    # and downloading its O and LSE inside the timed region.  The call
+    # pipelines them the way a serving loop runs them back to back: step i+1's
+    # upload and step i-1's download overlap step i's kernels (its own upload
+    # and download streams beside the compute stream, two device slots).
     q_p, k_p, v_p = (t.pin_memory() for t in (q_h, k_h, v_h))
     o_p = [torch.empty((B, H, N, D), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     lse_p = [torch.empty((B, H, N), dtype=torch.float32).pin_memory() for _ in range(2)]
-    ins = [(q, k, v), tuple(torch.empty_like(t) for t in (q, k, v))]
-    outs = [(o, lse), (torch.empty_like(o), torch.empty_like(lse))]
-    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev = {name: [torch.cuda.Event() for _ in range(2)] for name in ("up", "comp", "down")}
+    ws = fa.empty_host_batch_workspace((B, H, N, D), dev, causal=args.causal, fp8pv=args.fp8pv)
 
     def e2e_run(nsteps):
-        for i in range(nsteps):
-            sl = i % 2
-            qi, ki, vi = ins[sl]
-            oi, li = outs[sl]
-            if i >= 2:
-                up.wait_event(ev["comp"][sl])  # step i-2 has finished reading this input slot
-            with torch.cuda.stream(up):
-                qi.copy_(q_p, non_blocking=True)
-                ki.copy_(k_p, non_blocking=True)
-                vi.copy_(v_p, non_blocking=True)
-            ev["up"][sl].record(up)
-            stream.wait_event(ev["up"][sl])
-            if i >= 2:
-                stream.wait_event(ev["down"][sl])  # step i-2's outputs have left this slot
-            fa.quant_qk_nvfp4(qi, out=qq, stream=stream)
-            fa.quant_qk_nvfp4(ki, out=kq, stream=stream)
-            quant_v(vi, out=vq, stream=stream)
-            fwd(qq, kq, vq, w.softmax_scale, o=oi, lse=li, stream=stream)
-            ev["comp"][sl].record(stream)
-            down.wait_event(ev["comp"][sl])
-            with torch.cuda.stream(down):
-                o_p[sl].copy_(oi, non_blocking=True)
-                lse_p[sl].copy_(li, non_blocking=True)
-            ev["down"][sl].record(down)
+        fa.fwd_host_batch([q_p] * nsteps, [k_p] * nsteps, [v_p] * nsteps, [o_p[i % 2] for i in range(nsteps)],
+                          [lse_p[i % 2] for i in range(nsteps)], w.softmax_scale, causal=args.causal,
+                          fp8pv=args.fp8pv, workspace=ws, stream=stream)
 
     e2e_steps = max(4, args.steps)  # the same K steps as the device-timed region, fill and drain included
     e2e_run(2)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(up)
+    e0.record(stream)
     e2e_run(e2e_steps)
-    e1.record(down)
+    e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     if fa.device_status() != fa.FP4ATTN_OK:
@@ -643,6 +619,7 @@ def run_ours(args, w):
                      "kernel": "fwd_directp_kernel<%d, causal=%s, fp8pv=%s>"
                                % (D, str(bool(args.causal)).lower(), str(bool(args.fp8pv)).lower())},
         "e2e": {"value": whole_job_tflops(world, flops, e2e_ms), "unit": UNIT,
+                "api": "fp4attn_fwd_host_batch (C ABI, pinned host buffers in and out)",
                 "pipelining": "upload of step i+1 and download of step i-1 overlap step i's kernels",
                 "steps": e2e_steps, "timed": "first upload to last download (pipeline fill and drain included)",
                 "h2d_bytes_per_step": 3 * B * H * N * D * 2, "d2h_bytes_per_step": B * H * N * D * 2 + B * H * N * 4},
@@ -651,7 +628,7 @@ def run_ours(args, w):
     }
     if rank == 0 and world == 1 and not args.no_variants and args.workload == 4 and not args.causal \
             and not args.fp8pv:
-        del q, k, v, qq, kq, vq, o, lse, ins, outs, flush
+        del q, k, v, qq, kq, vq, o, lse, ws, flush
         torch.cuda.empty_cache()
         line["variants"] = [time_variant(wl.WORKLOADS[5], False, False, mma_peaks, dev, local),
                             time_variant(w, True, False, mma_peaks, dev, local),

@@ -93,6 +93,10 @@ def lib():
     L.fp4attn_bwd_prep.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
     L.fp4attn_bwd_directp_causal.argtypes = [ctypes.POINTER(_NVFP4), ctypes.POINTER(_NVFP4)] + \
         [ctypes.POINTER(_MXFP4)] * 5 + [vp, vp, vp, vp, vp, i, i, i, i, ctypes.c_float, vp]
+    L.fp4attn_fwd_host_batch_workspace_bytes.argtypes = [i, i, i, i, i, ctypes.POINTER(sz)]
+    L.fp4attn_fwd_host_batch.argtypes = [i, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                         ctypes.POINTER(vp), ctypes.POINTER(vp), i, i, i, i, ctypes.c_float, i,
+                                         vp, sz, vp]
     for name in ("fp4attn_debug_wait_timeout", "fp4attn_debug_mma_peak", "fp4attn_debug_noalloc_timeout",
                  "fp4attn_debug_status_word_exists", "fp4attn_mxfp8_v_bytes", "fp4attn_quant_v_mxfp8", "fp4attn_fwd_directp_fp8pv",
                  "fp4attn_debug_dump_p_fp8pv", "fp4attn_fwd_directp_causal", "fp4attn_debug_dump_p_causal", "fp4attn_fwd_directp_causal_save",
@@ -496,6 +500,66 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scale: 
     vq = quant_v_mxfp4(v, stream=stream)
     fwd = fwd_directp_causal if causal else fwd_directp
     return fwd(qq, kq, vq, softmax_scale, stream=stream)
+
+
+# ---- forwards from host memory -------------------------------------------------
+
+FP4ATTN_HB_CAUSAL, FP4ATTN_HB_FP8PV = 1, 2
+
+
+def _hb_flags(causal: bool, fp8pv: bool) -> int:
+    return (FP4ATTN_HB_CAUSAL if causal else 0) | (FP4ATTN_HB_FP8PV if fp8pv else 0)
+
+
+def host_batch_workspace_bytes(B, H, N, D, causal: bool = False, fp8pv: bool = False) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().fp4attn_fwd_host_batch_workspace_bytes(B, H, N, D, _hb_flags(causal, fp8pv), ctypes.byref(n)),
+           "fp4attn_fwd_host_batch_workspace_bytes")
+    return n.value
+
+
+def empty_host_batch_workspace(shape, device, causal: bool = False, fp8pv: bool = False) -> torch.Tensor:
+    """A device workspace for fwd_host_batch (u8, 256-byte aligned)."""
+    B, H, N, D = shape
+    ws = torch.empty((host_batch_workspace_bytes(B, H, N, D, causal, fp8pv),), dtype=torch.uint8, device=device)
+    if ws.data_ptr() % 256:
+        raise RuntimeError("the allocator returned a workspace that is not 256-byte aligned")
+    return ws
+
+
+def fwd_host_batch(qs, ks, vs, os_, lses, softmax_scale: float | None = None, causal: bool = False,
+                   fp8pv: bool = False, workspace: torch.Tensor | None = None, stream=None) -> None:
+    """fp4attn_fwd_host_batch: step i quantizes the host tensors qs[i], ks[i],
+    vs[i] (CPU bf16 [B,H,N,D], pinned for overlap) on the workspace's device,
+    runs the forward and writes os_[i] (CPU bf16) and lses[i] (CPU fp32
+    [B,H,N]).  Asynchronous on `stream`: the outputs are complete, and the
+    inputs free, once that stream has synchronised."""
+    n = len(qs)
+    if n < 1 or not (len(ks) == len(vs) == len(os_) == len(lses) == n):
+        raise ValueError("qs, ks, vs, os_ and lses must hold the same number (>= 1) of tensors")
+    shape = tuple(qs[0].shape)
+    if len(shape) != 4:
+        raise ValueError("inputs must be [B,H,N,D]")
+    B, H, N, D = shape
+    for seq, name, dtype, numel in ((qs, "qs", torch.bfloat16, B * H * N * D), (ks, "ks", torch.bfloat16, B * H * N * D),
+                                    (vs, "vs", torch.bfloat16, B * H * N * D), (os_, "os_", torch.bfloat16, B * H * N * D),
+                                    (lses, "lses", torch.float32, B * H * N)):
+        for j, t in enumerate(seq):
+            _check_buffer(t, "%s[%d]" % (name, j), dtype, numel, torch.device("cpu"))
+    if workspace is None:
+        raise ValueError("fwd_host_batch needs a device workspace (empty_host_batch_workspace)")
+    need = host_batch_workspace_bytes(B, H, N, D, causal, fp8pv)
+    if not (workspace.is_cuda and workspace.dtype == torch.uint8 and workspace.is_contiguous()
+            and workspace.numel() >= need):
+        raise ValueError("workspace must be a contiguous CUDA u8 tensor of at least %d bytes" % need)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    arr = lambda seq: (ctypes.c_void_p * n)(*[t.data_ptr() for t in seq])
+    with torch.cuda.device(workspace.device):
+        _check(lib().fp4attn_fwd_host_batch(n, arr(qs), arr(ks), arr(vs), arr(os_), arr(lses), B, H, N, D,
+                                            float(softmax_scale), _hb_flags(causal, fp8pv), _ptr(workspace),
+                                            workspace.numel(), ctypes.c_void_p(_stream(stream))),
+               "fp4attn_fwd_host_batch")
 
 
 # ---- causal backward ---------------------------------------------------------

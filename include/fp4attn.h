@@ -2,8 +2,9 @@
  * fp4attn -- Direct-P FP4 attention forward for GB300 (sm_103a).
  *
  * C ABI of the CUDA library libfp4attn.so.  Every call takes plain device
- * pointers and sizes, is asynchronous on the given CUDA stream (a
- * cudaStream_t passed as void*, NULL = legacy default stream), validates its
+ * pointers (fp4attn_fwd_host_batch also host buffers) and sizes, is
+ * asynchronous on the given CUDA stream (a cudaStream_t passed as void*,
+ * NULL = legacy default stream), validates its
  * arguments on the host before launching anything, and returns an
  * FP4ATTN_STATUS code.  The caller owns all input and output memory.  No call
  * allocates device memory, except that the first call on a device sets up a
@@ -380,6 +381,47 @@ int fp4attn_debug_wait_timeout(int limit_us, void *stream);
  * Errors: FP4ATTN_ERR_INVALID_ARG for kind outside 0..2 or iters outside
  * 1..2^26; a wait that gives up shows in fp4attn_device_status. */
 int fp4attn_debug_mma_peak(int kind, int iters, void *stream);
+
+/* Flags of fp4attn_fwd_host_batch: which forward each step runs. */
+enum {
+    FP4ATTN_HB_CAUSAL = 1, /* fp4attn_fwd_directp_causal (with FP8PV: causal FP8 P/V) */
+    FP4ATTN_HB_FP8PV = 2   /* MXFP8 V and fp4attn_fwd_directp_fp8pv */
+};
+
+/* Workspace size (bytes) of fp4attn_fwd_host_batch for one problem shape and
+ * flags: two slots of bf16 Q, K, V, O and fp32 LSE, plus one set of quantized
+ * Q, K (NVFP4) and V (MXFP4, or MXFP8 with FP4ATTN_HB_FP8PV), each region
+ * 256-byte aligned.  Errors: bad shape, null bytes or unknown flags. */
+int fp4attn_fwd_host_batch_workspace_bytes(int B, int H, int N, int D, int flags, size_t *bytes);
+
+/* The forward of nsteps independent problems of one shape, from HOST memory
+ * to HOST memory (the paper has no counterpart; this is the serving-loop form
+ * of the calls above: the abstract's forward, run on data that lives on the
+ * host).  Step i reads bf16 [B,H,N,D] q_h[i], k_h[i], v_h[i] and writes bf16
+ * o_h[i] and fp32 [B,H,N] lse_h[i]; it computes exactly what
+ * fp4attn_quant_qk_nvfp4 (Q, K), fp4attn_quant_v_mxfp4 or _mxfp8 (V) and the
+ * forward chosen by flags compute on device copies of those buffers.
+ * Pointer arrays and host buffers are the caller's; the host buffers must
+ * stay valid and untouched until the work completes (synchronise `stream`),
+ * and should be pinned (cudaHostAlloc / cudaHostRegister), or the copies
+ * do not overlap the kernels.  workspace: a device buffer of at least
+ * fp4attn_fwd_host_batch_workspace_bytes bytes, 256-byte aligned, owned by
+ * the caller and used by no other work until the call's work completes.
+ * Pipelining: an upload and a download stream of the call's own run beside
+ * `stream`, ordered by events, so step i+1's upload and step i-1's download
+ * overlap step i's kernels; the kernels run on `stream`, which is made to
+ * wait for the last download before the call returns, so events recorded on
+ * `stream` before and after the call span every copy.  All arguments are
+ * checked before anything is queued (FP4ATTN_ERR_INVALID_ARG / _UNSUPPORTED);
+ * a CUDA error while queueing stops the queueing and returns
+ * FP4ATTN_ERR_CUDA, with the work already queued still ordered before
+ * `stream`.  Bounded device-side waits that give up show in
+ * fp4attn_device_status.  Allocates no device memory; creates and releases
+ * two streams and eight events per call. */
+int fp4attn_fwd_host_batch(int nsteps, const void *const *q_h, const void *const *k_h, const void *const *v_h,
+                           void *const *o_h, float *const *lse_h, int B, int H, int N, int D,
+                           float softmax_scale, int flags, void *workspace, size_t workspace_bytes,
+                           void *stream);
 
 /* Reads and clears the status word the kernels of this library set when a
  * bounded device-side wait gives up (they then stop early and leave their

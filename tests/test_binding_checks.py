@@ -143,3 +143,27 @@ def test_backward_quantizer_and_prep_inputs(fa):
         fa.empty_fp8(SHAPE, "cols", fa.FP8_E4M3, "cpu")
     with pytest.raises(ValueError):
         fa.bwd_prep(x, x, torch.zeros(SHAPE[:3]))  # CPU inputs
+
+
+def test_host_batch_buffers_checked(fa):
+    B, H, N, D = SHAPE
+    x = [torch.zeros(SHAPE, dtype=torch.bfloat16)]
+    o = [torch.zeros(SHAPE, dtype=torch.bfloat16)]
+    lse = [torch.zeros((B, H, N), dtype=torch.float32)]
+    ws = torch.zeros((fa.host_batch_workspace_bytes(B, H, N, D),), dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        fa.fwd_host_batch(x, x, x, o, lse, workspace=ws)  # workspace not on a GPU
+    with pytest.raises(ValueError):
+        fa.fwd_host_batch(x, x, x, o, lse)  # no workspace
+    with pytest.raises(ValueError):
+        fa.fwd_host_batch(x, x, x + x, o, lse, workspace=ws)  # step counts differ
+    with pytest.raises(ValueError):
+        fa.fwd_host_batch([], [], [], [], [], workspace=ws)
+    with pytest.raises(ValueError):
+        fa.fwd_host_batch(x, x, [x[0].float()], o, lse, workspace=ws)  # not bf16
+    with pytest.raises(ValueError):
+        fa.fwd_host_batch(x, x, x, [o[0][:, :, :100]], lse, workspace=ws)  # short O
+    with pytest.raises(ValueError):
+        fa.fwd_host_batch(x, x, x, o, [lse[0].double()], workspace=ws)  # LSE not fp32
+    with pytest.raises(ValueError):
+        fa.fwd_host_batch(x, x, x, o, lse, workspace=ws[:-1])  # workspace too small (checked first as CPU)

@@ -198,3 +198,50 @@ def test_backward_argument_errors_without_gpu(L):
     assert call(scale=float("nan")) == fa.FP4ATTN_ERR_INVALID_ARG
     assert call(scale=-1.0) == fa.FP4ATTN_ERR_INVALID_ARG
     assert call(D=32) == fa.FP4ATTN_ERR_UNSUPPORTED
+
+
+def test_host_batch_workspace_and_argument_errors_without_gpu(L):
+    import blackwell_nvfp4_quantize_gb300 as fa
+
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    # two slots of bf16 Q, K, V, O and fp32 LSE; NVFP4 Q and K (payload,
+    # atoms, 4-byte g, each region 256-aligned); V payload and atoms
+    for (B, H, N, D) in [(1, 40, 32768, 128), (2, 3, 77, 64)]:
+        tiles = (N + 127) // 128
+        slot = 4 * up(B * H * N * D * 2) + up(B * H * N * 4)
+        qk = up(B * H * N * D // 2) + up(B * H * tiles * (D // 64) * 512) + 256
+        for fp8pv in (False, True):
+            vpay = up(B * H * D * tiles * (128 if fp8pv else 64))
+            want = 2 * slot + 2 * qk + vpay + up(B * H * tiles * 512)
+            for causal in (False, True):
+                assert fa.host_batch_workspace_bytes(B, H, N, D, causal, fp8pv) == want
+    sz = ctypes.c_size_t()
+    assert L.fp4attn_fwd_host_batch_workspace_bytes(1, 1, 128, 64, 4, ctypes.byref(sz)) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert L.fp4attn_fwd_host_batch_workspace_bytes(1, 1, 128, 64, 0, None) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert L.fp4attn_fwd_host_batch_workspace_bytes(1, 1, 128, 80, 0, ctypes.byref(sz)) == fa.FP4ATTN_ERR_UNSUPPORTED
+
+    # the batch call: everything is checked before a stream is made or a copy queued
+    need = fa.host_batch_workspace_bytes(1, 1, 128, 64)
+    h = ctypes.c_void_p(0x7000)
+    arr = lambda *p: (ctypes.c_void_p * len(p))(*p)
+    two = arr(h, h)
+    hole = arr(h, None)
+
+    def call(n=2, q=two, k=two, v=two, o=two, lse=two, D=64, scale=0.125, flags=0, ws=0x100000, nbytes=need):
+        return L.fp4attn_fwd_host_batch(n, q, k, v, o, lse, 1, 1, 128, D, ctypes.c_float(scale), flags,
+                                        ctypes.c_void_p(ws), nbytes, None)
+
+    assert call(n=0) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert call(q=None) == fa.FP4ATTN_ERR_INVALID_ARG
+    for name in ("q", "k", "v", "o", "lse"):
+        assert call(**{name: hole}) == fa.FP4ATTN_ERR_INVALID_ARG, name
+    assert call(flags=4) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert call(scale=float("inf")) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert call(scale=0.0) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert call(ws=0) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert call(ws=0x100010) == fa.FP4ATTN_ERR_INVALID_ARG          # not 256-aligned
+    assert call(nbytes=need - 1) == fa.FP4ATTN_ERR_INVALID_ARG
+    assert call(flags=fa.FP4ATTN_HB_FP8PV) == fa.FP4ATTN_ERR_INVALID_ARG  # the FP8 V needs more bytes
+    assert call(D=96) == fa.FP4ATTN_ERR_UNSUPPORTED
