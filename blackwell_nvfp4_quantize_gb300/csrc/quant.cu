@@ -6,7 +6,7 @@
 //  nvfp4_quant_kernel : 16-element blocks along D, E4M3 block scale, E2M1 codes
 //  nvfp4_finalize     : g = amax / 2688 (1 for an all-zero tensor)
 //  mxfp4_v_kernel     : 32-key blocks per channel, E8M0 scale, codes written
-//                       key-inner (V transposed) through shared memory
+//                       key-inner (V transposed)
 //  mxfp8_t_kernel     : the same for FP8 codes, one byte per token: E4M3 V of
 //                       the FP8 P/V variant (training keeps FP8 probabilities
 //                       and values) and the backward's sequence-blocked
@@ -16,8 +16,9 @@
 //
 // The data kernels are HBM-bound streaming passes: 16-byte vector loads with
 // 4 to 16 of them in flight per thread (a read stream on this GPU needs about
-// 8 to approach the DRAM peak), grids in multiples of the SM count,
-// warp-shuffle reductions and coalesced stores.  fp32 arithmetic uses explicitly rounded intrinsics so that
+// 8 to approach the DRAM peak; the transposing kernels keep 32 coalesced
+// 4-byte loads in flight per thread instead), grids in multiples of the SM
+// count, warp-shuffle reductions and coalesced stores.  fp32 arithmetic uses explicitly rounded intrinsics so that
 // no multiply-add contraction changes a code.
 #include <cuda_bf16.h>
 
@@ -172,50 +173,43 @@ __global__ void __launch_bounds__(256) nvfp4_quant_kernel(const uint4* __restric
 
 __global__ void nvfp4_finalize_kernel(float* g) { *g = global_scale(*g); }
 
-// The 128 token rows of key tile kt of head bh (rows past N as zeros) into
-// shared memory, row-major: the tile is one contiguous stretch of V, and each
-// of the 256 threads has all of its 16-byte loads in flight before its first
-// store.
+// Channels d0, d0 + 1 of keys key0 .. key0 + 31 of head bh as 32-bit words
+// (one per key; keys >= N read 0).  The lanes of a warp take consecutive
+// channel pairs of the same keys, so each of the 32 loads, all in flight at
+// once, reads 128 contiguous bytes of one key row.
 template <int D>
-__device__ __forceinline__ void stage_v_tile(const uint4* __restrict__ v, uint16_t* tile, int kt, long long bh,
-                                             int N) {
-  constexpr int VPR = D / 8;                   // 16-byte vectors per token row
-  constexpr int kPerThread = 128 * VPR / 256;  // 8 (D = 128) or 4 (D = 64)
-  const uint4* src = v + (bh * N + static_cast<long long>(kt) * 128) * VPR;
-  const int rows = N - kt * 128 < 128 ? N - kt * 128 : 128;
-  uint4 val[kPerThread];
+__device__ __forceinline__ void load_pair_block(const uint4* __restrict__ v, long long bh, int N, int key0, int d0,
+                                                uint32_t (&w2)[32]) {
+  const int nk = N - key0;
+  const uint32_t* col = reinterpret_cast<const uint32_t*>(v) + ((bh * N + key0) * D + d0) / 2;
 #pragma unroll
-  for (int u = 0; u < kPerThread; ++u) {
-    const int i = threadIdx.x + 256 * u;
-    val[u] = (i / VPR < rows) ? ld_stream(src + i) : make_uint4(0u, 0u, 0u, 0u);
+  for (int i = 0; i < 32; ++i) {
+    uint32_t x = 0u;
+    if (i < nk) asm volatile("ld.global.nc.L1::no_allocate.L2::256B.u32 %0, [%1];" : "=r"(x) : "l"(col + i * (D / 2)));
+    w2[i] = x;
   }
-#pragma unroll
-  for (int u = 0; u < kPerThread; ++u) reinterpret_cast<uint4*>(tile)[threadIdx.x + 256 * u] = val[u];
 }
 
 // V [B,H,N,D] bf16 -> V^T codes [B,H,D,Npad/2] + E8M0 atoms.  One CTA per
-// (128-key tile, b*H+h).  The tile is staged in shared memory row-major;
-// lanes of a warp then take consecutive channels d of one 32-key block, so
-// each column read is conflict-free.
+// (128-key tile, b*H+h); a thread takes the channel pair (d, d+1) of one
+// 32-key block straight from global memory (no staging: the loads of a warp
+// are coalesced key rows) and writes each channel's 16 code bytes with a
+// plain write-back store, so L2 joins them with the neighbouring blocks'
+// halves of each 32-byte sector before they reach DRAM.
 template <int D>
 __global__ void __launch_bounds__(256) mxfp4_v_kernel(const uint4* __restrict__ v, uint8_t* __restrict__ payload_t,
                                                       uint8_t* __restrict__ sf, int N) {
-  __shared__ __align__(16) uint16_t tile[128 * D];
   __shared__ __align__(16) uint32_t atom[128];
   const int kt = blockIdx.x;
   const long long bh = blockIdx.y;
   const int ntiles = gridDim.x;
   const int npad_half = ntiles * 64;  // bytes per V^T row
-  stage_v_tile<D>(v, tile, kt, bh, N);
   if (threadIdx.x < 128) atom[threadIdx.x] = 0u;
   __syncthreads();
-  // a thread takes the channel pair (d, d+1) of one 32-key block: one 32-bit
-  // shared read per key, consecutive lanes on consecutive words
   for (int pidx = threadIdx.x; pidx < 2 * D; pidx += 256) {
     const int d0 = 2 * (pidx % (D / 2)), kb = pidx / (D / 2);
     uint32_t w2[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) w2[i] = *reinterpret_cast<const uint32_t*>(&tile[(kb * 32 + i) * D + d0]);
+    load_pair_block<D>(v, bh, N, kt * 128 + kb * 32, d0, w2);
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const int d = d0 + c;
@@ -236,7 +230,7 @@ __global__ void __launch_bounds__(256) mxfp4_v_kernel(const uint4* __restrict__ 
       out.y = cvt_e2m1x8(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]);
       out.z = cvt_e2m1x8(y[16], y[17], y[18], y[19], y[20], y[21], y[22], y[23]);
       out.w = cvt_e2m1x8(y[24], y[25], y[26], y[27], y[28], y[29], y[30], y[31]);
-      __stcs(reinterpret_cast<uint4*>(payload_t + (bh * D + d) * npad_half + kt * 64 + kb * 16), out);
+      *reinterpret_cast<uint4*>(payload_t + (bh * D + d) * npad_half + kt * 64 + kb * 16) = out;
       reinterpret_cast<uint8_t*>(atom)[(d & 31) * 16 + (d >> 5) * 4 + kb] = static_cast<uint8_t>(e + 127);
     }
   }
@@ -246,26 +240,23 @@ __global__ void __launch_bounds__(256) mxfp4_v_kernel(const uint4* __restrict__ 
         reinterpret_cast<const uint4*>(atom)[threadIdx.x];
 }
 
-// MXFP8 along the sequence, transposed: the same staging and atoms as
+// MXFP8 along the sequence, transposed: the same loads, stores and atoms as
 // mxfp4_v_kernel; the scale is the smallest 2^e with amax <= fmt_max * 2^e
 // and each token keeps one FP8 byte.
 template <int D, int FMT>
 __global__ void __launch_bounds__(256) mxfp8_t_kernel(const uint4* __restrict__ v, uint8_t* __restrict__ payload_t,
                                                       uint8_t* __restrict__ sf, int N) {
-  __shared__ __align__(16) uint16_t tile[128 * D];
   __shared__ __align__(16) uint32_t atom[128];
   const int kt = blockIdx.x;
   const long long bh = blockIdx.y;
   const int ntiles = gridDim.x;
   const int npad = ntiles * 128;  // bytes per transposed row
-  stage_v_tile<D>(v, tile, kt, bh, N);
   if (threadIdx.x < 128) atom[threadIdx.x] = 0u;
   __syncthreads();
   for (int pidx = threadIdx.x; pidx < 2 * D; pidx += 256) {  // channel pairs, as in mxfp4_v_kernel
     const int d0 = 2 * (pidx % (D / 2)), kb = pidx / (D / 2);
     uint32_t w2[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) w2[i] = *reinterpret_cast<const uint32_t*>(&tile[(kb * 32 + i) * D + d0]);
+    load_pair_block<D>(v, bh, N, kt * 128 + kb * 32, d0, w2);
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const int d = d0 + c;
@@ -282,8 +273,8 @@ __global__ void __launch_bounds__(256) mxfp8_t_kernel(const uint4* __restrict__ 
 #pragma unroll
       for (int i = 0; i < 8; ++i) wd[i] = cvt_fp8x4<FMT>(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
       uint4* dst = reinterpret_cast<uint4*>(payload_t + (bh * D + d) * npad + kt * 128 + kb * 32);
-      __stcs(dst, make_uint4(wd[0], wd[1], wd[2], wd[3]));
-      __stcs(dst + 1, make_uint4(wd[4], wd[5], wd[6], wd[7]));
+      dst[0] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+      dst[1] = make_uint4(wd[4], wd[5], wd[6], wd[7]);
       reinterpret_cast<uint8_t*>(atom)[(d & 31) * 16 + (d >> 5) * 4 + kb] = static_cast<uint8_t>(e + 127);
     }
   }
