@@ -214,12 +214,19 @@ def cpu_baseline(w, q, k, v, causal=False, fp8pv=False, budget_s=12.0):
     vq = oracle.quant_mxfp8_v(vb, threads) if fp8pv else oracle.quant_mxfp4_v(vb, threads)
     pv_fmt = oracle.PV_MXFP8 if fp8pv else oracle.PV_MXFP4
     t_quant = time.perf_counter() - t0
-    # calibrate, then time a sample sized to the budget
-    probe = np.linspace(0, N - 1, min(N, 2 * threads)).astype(np.int64)
-    t0 = time.perf_counter()
-    oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, probe, threads, causal=causal, pv_fmt=pv_fmt)
-    t_probe = time.perf_counter() - t0
-    rows = int(max(len(probe), min(N, len(probe) * budget_s / max(t_probe, 1e-6))))
+    # calibrate in two stages (a tiny probe overstates the per-row cost: the
+    # thread pool's start-up dominates it), then time a sample sized to the budget
+    def timed_rows(n):
+        r = np.linspace(0, N - 1, n).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, r, threads, causal=causal, pv_fmt=pv_fmt)
+        return time.perf_counter() - t0
+
+    n1 = min(N, 2 * threads)
+    t1 = timed_rows(n1)
+    n2 = int(max(n1, min(N, n1 * 1.5 / max(t1, 1e-6))))
+    t2 = timed_rows(n2) if n2 > n1 else t1
+    rows = int(max(n2, min(N, n2 * budget_s / max(t2, 1e-6))))
     sample = np.linspace(0, N - 1, rows).astype(np.int64)
     t0 = time.perf_counter()
     oracle.directp_rows(qq, kq, vq, shape1, w.softmax_scale, sample, threads, causal=causal, pv_fmt=pv_fmt)
