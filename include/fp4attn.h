@@ -406,7 +406,8 @@ int fp4attn_fwd_host_batch_workspace_bytes(int B, int H, int N, int D, int flags
  * and should be pinned (cudaHostAlloc / cudaHostRegister), or the copies
  * do not overlap the kernels.  workspace: a device buffer of at least
  * fp4attn_fwd_host_batch_workspace_bytes bytes, 256-byte aligned, owned by
- * the caller and used by no other work until the call's work completes.
+ * the caller and used by no other work until the call's work completes; it,
+ * `stream` and the call's own streams belong to the current device.
  * Pipelining: an upload and a download stream of the call's own run beside
  * `stream`, ordered by events, so step i+1's upload and step i-1's download
  * overlap step i's kernels; the kernels run on `stream`, which is made to
