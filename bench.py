@@ -12,7 +12,14 @@ quoted on.  Its inputs (1 GB bf16, 0.28 GB quantized) exceed the 129 MB L2, so
 no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload I] [--causal]
+                  [--workload I] [--causal] [--fp8pv] [--bwd]
+                  [--no-variants] [--no-cpu-baseline]
+
+"e2e" repeats the K steps from pinned host memory through the C ABI's
+host-buffer call (fp4attn_fwd_host_batch): every step's upload of Q, K, V
+and download of O and LSE run inside the timed region, pipelined across
+steps.  --bwd prints the causal backward's line alone (FP8 operand
+quantizers, prep pass and the two backward kernels per step).
 
 --impl reference times the CPU oracle (the plain C restatement used by the
 tests) on a bounded sample of the same workload; it is a reported baseline.
@@ -27,7 +34,9 @@ the FP8 P/V variant), one CTA per SM (fp4attn_debug_mma_peak).  The forward
 spends half its FLOPs in each product, so its peak is the FLOP-weighted
 harmonic combination of the two rates.  The default run also times the
 forward of the D=64 workload and the causal and FP8 P/V forwards on the
-default workload, reported in "variants" of the same JSON line.
+default workload and the causal backward, reported in "variants" of the
+same JSON line (--no-variants skips them; --no-cpu-baseline skips the timed
+oracle sample).
 
   python bench.py --mma-peak   prints the measured peaks and the clocks seen
 """
