@@ -203,7 +203,7 @@ def whole_job_tflops(world, flops_per_replica, ms):
     return world * flops_per_replica / (ms * 1e-3) / 1e12
 
 
-def cpu_baseline(w, q, k, v, causal=False, fp8pv=False, budget_s=12.0):
+def cpu_baseline(w, q, k, v, causal=False, fp8pv=False, budget_s=16.0):
     """The oracle as it stands, on host cores, on a bounded row sample of head 0."""
     import numpy as np
 
@@ -583,6 +583,17 @@ def run_ours(args, w):
     e2e_steps = max(4, args.steps)  # the same K steps as the device-timed region, fill and drain included
     e2e_run(2)
     barrier()
+    # the host link as this run sees it (the GPU's neighbours on the machine
+    # share its host memory): one pinned upload and one download of Q's bytes
+    link = {}
+    for name, dst, src in (("h2d", q, q_p), ("d2h", q_p, q)):
+        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        l0.record(stream)
+        dst.copy_(src, non_blocking=True)
+        l1.record(stream)
+        l1.synchronize()
+        link[name] = round(q.numel() * 2 / (l0.elapsed_time(l1) * 1e-3) / 1e9, 1)
+    barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     e2e_run(e2e_steps)
@@ -638,7 +649,8 @@ def run_ours(args, w):
                 "api": "fp4attn_fwd_host_batch (C ABI, pinned host buffers in and out)",
                 "pipelining": "upload of step i+1 and download of step i-1 overlap step i's kernels",
                 "steps": e2e_steps, "timed": "first upload to last download (pipeline fill and drain included)",
-                "h2d_bytes_per_step": 3 * B * H * N * D * 2, "d2h_bytes_per_step": B * H * N * D * 2 + B * H * N * 4},
+                "h2d_bytes_per_step": 3 * B * H * N * D * 2, "d2h_bytes_per_step": B * H * N * D * 2 + B * H * N * 4,
+                "host_link_gbs": link},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }
